@@ -1,0 +1,201 @@
+"""Plain fp64 CPU oracle for the grouped MoE backward GEMMs.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+(``moe_grouped_gemm_wgrad_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, no blocking); this module
+compiles it with gcc on first use and wraps it with ctypes over numpy arrays.
+Each function's docstring names the passage of the pages it restates:
+
+* wgrad page: "tinygrad/extra/thunder/amd/grouped_mxfp8_wgrad.cpp"
+* dgrad page: "oarust ... grouped_gemm_m_data_backward.slang"
+* post-attn page: vLLM "models/minimax_m3/amd/mono/kernels/post_attn" (the
+  saturating clamp of its MXFP8 quantizer, mx8_q)
+* OCP "OFP8 Formats" v1.0 and "Microscaling Formats (MX)" v1.0 for the codecs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` beside it (plain gcc, no -ffast-math,
+    no FMA contraction, so x86 and aarch64 give the same results)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "oracle.h"))
+    ):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+             "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i32, i64, u8, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_uint8, ctypes.c_double
+            lib.orc_e4m3_decode.argtypes = [u8]
+            lib.orc_e4m3_decode.restype = dbl
+            lib.orc_e4m3_encode_rne_satfinite.argtypes = [dbl]
+            lib.orc_e4m3_encode_rne_satfinite.restype = u8
+            lib.orc_e8m0_decode.argtypes = [u8]
+            lib.orc_e8m0_decode.restype = dbl
+            lib.orc_mx_scale_byte.argtypes = [dbl]
+            lib.orc_mx_scale_byte.restype = u8
+            lib.orc_padded_starts.argtypes = [P, i32, P]
+            lib.orc_padded_starts.restype = None
+            lib.orc_mxfp8_quantize.argtypes = [P, i32, i32, P, i32, i64, P, P]
+            lib.orc_mxfp8_quantize.restype = None
+            lib.orc_grouped_wgrad.argtypes = [P, P, P, P, P, i32, i32, i32, i64, P]
+            lib.orc_grouped_wgrad.restype = None
+            lib.orc_grouped_wgrad_element.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32]
+            lib.orc_grouped_wgrad_element.restype = dbl
+            lib.orc_expert_for_row_scan.argtypes = [P, i32, i32]
+            lib.orc_expert_for_row_scan.restype = i32
+            lib.orc_expert_for_row_bsearch.argtypes = [P, i32, i32]
+            lib.orc_expert_for_row_bsearch.restype = i32
+            lib.orc_grouped_dgrad.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
+            lib.orc_grouped_dgrad.restype = None
+            lib.orc_grouped_dgrad_element.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
+            lib.orc_grouped_dgrad_element.restype = dbl
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> ctypes.c_void_p:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _off(expert_off) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(expert_off, dtype=np.int32))
+
+
+# ------------------------------------------------------------------ codecs
+def e4m3_decode(b: int) -> float:
+    """OCP OFP8 E4M3 value of one byte (NaN for S.1111.111)."""
+    return _load().orc_e4m3_decode(int(b) & 0xFF)
+
+
+def e4m3_encode(v: float) -> int:
+    """Round-to-nearest-even to E4M3, saturating at +-448 (post-attn page, mx8_q clamp)."""
+    return int(_load().orc_e4m3_encode_rne_satfinite(float(v)))
+
+
+def e8m0_decode(b: int) -> float:
+    """OCP MX E8M0 value 2^(b-127)."""
+    return _load().orc_e8m0_decode(int(b) & 0xFF)
+
+
+def mx_scale_byte(amax: float) -> int:
+    """E8M0 byte of 2^(floor(log2 amax) - 8), clamped to the E8M0 range; 0 for amax 0."""
+    return int(_load().orc_mx_scale_byte(float(amax)))
+
+
+def padded_starts(expert_off) -> np.ndarray:
+    """P[e]: start of expert e's 128-padded segment in the quantized token axis."""
+    off = _off(expert_off)
+    E = off.size - 1
+    P = np.zeros(E + 1, dtype=np.int64)
+    _load().orc_padded_starts(_ptr(off), E, _ptr(P))
+    return P
+
+
+def token_capacity(M: int, E: int) -> int:
+    """Smallest padded token axis that fits any split of M tokens over E experts."""
+    return (M + 127 * E + 127) // 128 * 128
+
+
+# ---------------------------------------------------------------- quantize
+def mxfp8_quantize(src_bf16_bits: np.ndarray, expert_off, Mcap: int | None = None):
+    """MXFP8 quantization along the token axis (wgrad page: A = g^T, B = x^T in e4m3
+    with e8m0 scales per 32 tokens).  ``src_bf16_bits`` is uint16 [M, C].
+
+    Returns (q [C, Mcap] uint8, sc [C, Mcap/32] uint8) in the plain layout."""
+    src = np.ascontiguousarray(src_bf16_bits, dtype=np.uint16)
+    M, C = src.shape
+    off = _off(expert_off)
+    E = off.size - 1
+    if Mcap is None:
+        Mcap = token_capacity(M, E)
+    q = np.empty((C, Mcap), dtype=np.uint8)
+    sc = np.empty((C, Mcap // 32), dtype=np.uint8)
+    _load().orc_mxfp8_quantize(_ptr(src), M, C, _ptr(off), E, Mcap, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+# ------------------------------------------------------------------- wgrad
+def grouped_wgrad(gq, gs, xq, xs, expert_off) -> np.ndarray:
+    """fp64 grad_w [E*N, K] = per expert g_e^T x_e over its tokens (wgrad page)."""
+    off = _off(expert_off)
+    E = off.size - 1
+    N, Mcap = gq.shape
+    K = xq.shape[0]
+    out = np.empty((E * N, K), dtype=np.float64)
+    _load().orc_grouped_wgrad(_ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(off), E, N, K,
+                              Mcap, _ptr(out))
+    return out
+
+
+def grouped_wgrad_element(gq, gs, xq, xs, expert_off, e: int, n: int, k: int) -> float:
+    """One element grad_w[e*N + n, k] of :func:`grouped_wgrad`."""
+    off = _off(expert_off)
+    return _load().orc_grouped_wgrad_element(_ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(off),
+                                             off.size - 1, gq.shape[1], e, n, k)
+
+
+# ------------------------------------------------------------------- dgrad
+def expert_for_row_scan(expert_off, row: int) -> int:
+    """The dgrad page's expert_for_row (linear scan)."""
+    off = _off(expert_off)
+    return int(_load().orc_expert_for_row_scan(_ptr(off), off.size - 1, row))
+
+
+def expert_for_row_bsearch(expert_off, row: int) -> int:
+    """Binary-search restatement of the same rule."""
+    off = _off(expert_off)
+    return int(_load().orc_expert_for_row_bsearch(_ptr(off), off.size - 1, row))
+
+
+def grouped_dgrad(dy: np.ndarray, W: np.ndarray, expert_off):
+    """fp64 dx[r] = dy[r] . W[e(r)] and bound = |dy| . |W[e(r)]| (dgrad page)."""
+    dy = np.ascontiguousarray(dy, dtype=np.float32)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    off = _off(expert_off)
+    rows, out_f = dy.shape
+    E, _, in_f = W.shape
+    dx = np.empty((rows, in_f), dtype=np.float64)
+    bound = np.empty((rows, in_f), dtype=np.float64)
+    _load().orc_grouped_dgrad(_ptr(dy), _ptr(W), _ptr(off), E, rows, out_f, in_f, _ptr(dx),
+                              _ptr(bound))
+    return dx, bound
+
+
+def grouped_dgrad_element(dy: np.ndarray, W: np.ndarray, expert_off, r: int, k: int):
+    """(dx[r, k], bound[r, k]) of :func:`grouped_dgrad`, one element."""
+    off = _off(expert_off)
+    rows, out_f = dy.shape
+    E, _, in_f = W.shape
+    b = ctypes.c_double(0.0)
+    v = _load().orc_grouped_dgrad_element(_ptr(dy), _ptr(W), _ptr(off), E, rows, out_f, in_f,
+                                          r, k, ctypes.c_void_p(ctypes.addressof(b)))
+    return v, b.value

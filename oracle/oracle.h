@@ -1,0 +1,76 @@
+/*
+ * Plain CPU oracle for the grouped MoE backward GEMMs (MXFP8 wgrad, fp32 dgrad,
+ * MXFP8 quantization).  TEST INFRASTRUCTURE ONLY: nothing on the product path
+ * may include, link or call this code.  It shares no source with the CUDA
+ * library; it is slow on purpose, fp64 throughout, with no blocking, fusion or
+ * reordering beyond the plain definitions.
+ *
+ * Sources (page titles as cited in the docstrings below):
+ *   [wgrad page]  tinygrad/extra/thunder/amd/grouped_mxfp8_wgrad.cpp
+ *   [dgrad page]  oarust grouped_gemm_m_data_backward.slang
+ *   [post-attn page] vLLM MiniMax-M3 AMD post_attn kernels (quantization rule)
+ *   OCP "OFP8 Formats" v1.0 and OCP "Microscaling Formats (MX)" v1.0.
+ *
+ * Every function here is pinned by tests in tests/test_oracle_*.py against
+ * values fixed by the pages or by mathematics; none is "parity unpinned".
+ */
+#ifndef MGW_ORACLE_H
+#define MGW_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* OCP OFP8 E4M3: value of one byte (NaN for S.1111.111). */
+double orc_e4m3_decode(uint8_t b);
+/* OCP OFP8 E4M3: round-to-nearest-even of v, saturating |v| beyond 448 to 448. */
+uint8_t orc_e4m3_encode_rne_satfinite(double v);
+/* OCP MX E8M0: 2^(b-127); NaN for 255. */
+double orc_e8m0_decode(uint8_t b);
+/* MX shared-exponent rule for one block: byte of 2^(floor(log2 amax) - 8),
+ * clamped to [-127, 127] before the +127 bias; amax == 0 gives byte 0. */
+uint8_t orc_mx_scale_byte(double amax);
+/* bf16 bit pattern -> exact value. */
+double orc_bf16_decode(uint16_t h);
+
+/* 128-padded start of each expert's token segment in the quantized layout:
+ * P[0] = 0, P[e+1] = P[e] + ceil128(off[e+1] - off[e]).  Writes E+1 entries. */
+void orc_padded_starts(const int32_t *off, int E, int64_t *P);
+
+/* MXFP8 quantization of a bf16 [M, C] row-major matrix along the token axis,
+ * blocks of 32 tokens restarting at each expert's first token.
+ *   q  : [C, Mcap] e4m3 bytes, token-contiguous, expert e at P[e]; pads 0.
+ *   sc : [C, Mcap/32] e8m0 bytes (plain layout), block j of expert e at
+ *        P[e]/32 + j; pads 0. */
+void orc_mxfp8_quantize(const uint16_t *src, int M, int C, const int32_t *off, int E,
+                        int64_t Mcap, uint8_t *q, uint8_t *sc);
+
+/* Grouped wgrad: out[(e*N+n)*K + k] = sum_{t<cnt_e} deq(g)[n, P_e+t] * deq(x)[k, P_e+t]
+ * in fp64, from the quantized operands (q and plain scales as above). */
+void orc_grouped_wgrad(const uint8_t *gq, const uint8_t *gs, const uint8_t *xq,
+                       const uint8_t *xs, const int32_t *off, int E, int N, int K,
+                       int64_t Mcap, double *out);
+/* One element of the same (for sampled checks at full size). */
+double orc_grouped_wgrad_element(const uint8_t *gq, const uint8_t *gs, const uint8_t *xq,
+                                 const uint8_t *xs, const int32_t *off, int E, int64_t Mcap,
+                                 int e, int n, int k);
+
+/* Row -> expert rule of the dgrad page (linear scan over offsets[1..E-1]). */
+int orc_expert_for_row_scan(const int32_t *off, int E, int row);
+/* Same rule by binary search: the last e in [0, E) with off[e] <= row, taking the
+ * largest such e (so empty experts are skipped). */
+int orc_expert_for_row_bsearch(const int32_t *off, int E, int row);
+
+/* Grouped dgrad: dx[r,k] = sum_n dy[r,n] * W[e(r), n, k] in fp64, and
+ * bound[r,k] = sum_n |dy[r,n]| * |W[e(r),n,k]|.  bound may be NULL. */
+void orc_grouped_dgrad(const float *dy, const float *W, const int32_t *off, int E, int rows,
+                       int out_f, int in_f, double *dx, double *bound);
+/* One element of the same; *bound_out may be NULL. */
+double orc_grouped_dgrad_element(const float *dy, const float *W, const int32_t *off, int E,
+                                 int rows, int out_f, int in_f, int r, int k, double *bound_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
