@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped MoE backward GEMMs on one GB300 (or N replicas).
+
+Default workload: MXFP8 grouped wgrad at the wgrad page's default shape,
+M = N = K = 8192 tokens/features, E = 8 experts of 1024 tokens.  One step is the
+whole hot path for that workload: MXFP8 quantize of g and of x, then the grouped
+wgrad.  ``value`` is algorithmic wgrad FLOPs (2*M*N*K) per second of step time.
+A secondary object measures the fp32 grouped dgrad (rows 4096, 1024 -> 1024,
+E = 8, multinomial split).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "moe_grouped_gemm_wgrad_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, src_files) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary, if taken on this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        ent = t[kernel]
+        if ent.get("source_hash") == _source_hash(src_files):
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str | None):
+        self.proc = None
+        self.path = path
+        self.gpu = gpu_index
+        if path is None:
+            return
+        try:
+            self.fh = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workloads
+def wgrad_case(name):
+    from moe_grouped_gemm_wgrad_gb300 import synth
+
+    if name == "moe_ffn_pair":
+        return synth.moe_ffn_pair()[0]
+    return getattr(synth, name)()
+
+
+def dgrad_case(name):
+    from moe_grouped_gemm_wgrad_gb300 import synth
+
+    if name == "moe_ffn_pair":
+        return synth.moe_ffn_pair()[1]
+    return getattr(synth, name)()
+
+
+def run_wgrad(name, steps, warmup, dist_ctx):
+    import torch
+
+    from moe_grouped_gemm_wgrad_gb300 import mgw
+
+    case = wgrad_case(name)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M, N, K, E = case.M, case.N, case.K, case.E
+    flops = 2.0 * M * N * K
+    Mcap = mgw.token_capacity(M, E)
+    g_host = torch.from_numpy(case.g_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x_host = torch.from_numpy(case.x_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    off_host = torch.from_numpy(case.expert_off).pin_memory()
+    g = g_host.to(dev)
+    x = x_host.to(dev)
+    off = off_host.to(dev)
+    gq = torch.empty((N, Mcap), dtype=torch.uint8, device=dev)
+    xq = torch.empty((K, Mcap), dtype=torch.uint8, device=dev)
+    gs = torch.empty((mgw.scale_bytes(N, Mcap),), dtype=torch.uint8, device=dev)
+    xs = torch.empty((mgw.scale_bytes(K, Mcap),), dtype=torch.uint8, device=dev)
+    out = torch.empty((E * N, K), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mgw.mxfp8_quantize(g, off, Mcap, gq, gs, status)
+        mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)
+        mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    # per-kernel events inside the timed region, on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dist_ctx.local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_r{dist_ctx.rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        mgw.mxfp8_quantize(g, off, Mcap, gq, gs, status)
+        ev[i][1].record(stream)
+        mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)
+        ev[i][2].record(stream)
+        mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
+        ev[i][3].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    clk = clocks.stop()
+    total_ms = dist_ctx.max(t_start.elapsed_time(t_end))
+    wg_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    qg_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    qx_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    # end to end through the public API: pinned host inputs in, grad_w out to host
+    out_host = torch.empty((E * N, K), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(steps, 20))
+
+    def e2e_step():
+        g.copy_(g_host, non_blocking=True)
+        x.copy_(x_host, non_blocking=True)
+        off.copy_(off_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_ctx.max(a.elapsed_time(b)) / e2e_steps
+    h2d = g_host.numel() * 2 + x_host.numel() * 2 + off_host.numel() * 4
+    d2h = out_host.numel() * 2
+
+    ms_step = total_ms / steps
+    wg_avg = statistics.mean(wg_ms)
+    bytes_q = lambda C: M * C * 2 + C * Mcap + C * Mcap // 32  # noqa: E731
+    return {
+        "case": case, "flops": flops, "ms_per_step": ms_step, "wgrad_ms": wg_avg,
+        "wgrad_ms_median": statistics.median(wg_ms), "quant_g_ms": statistics.mean(qg_ms),
+        "quant_x_ms": statistics.mean(qx_ms), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+        "clocks": clk, "launches": 3 * steps,
+        "quant_bytes": bytes_q(N) + bytes_q(K),
+        "wgrad_min_bytes": N * Mcap + K * Mcap + (N + K) * Mcap // 32 + E * N * K * 2,
+    }
+
+
+def run_dgrad(name, steps, warmup):
+    import torch
+
+    from moe_grouped_gemm_wgrad_gb300 import mgw
+
+    case = dgrad_case(name)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dy = torch.from_numpy(case.dy).to(dev)
+    W = torch.from_numpy(case.W).to(dev)
+    off = torch.from_numpy(case.expert_off).to(dev)
+    dx = torch.empty((case.rows, case.in_f), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        mgw.grouped_dgrad_f32(dy, W, off, dx)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1.0)  # L2 flush between timed launches (256 MB > 129 MB L2)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        mgw.grouped_dgrad_f32(dy, W, off, dx)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in times]
+    flops = 2.0 * case.rows * case.out_f * case.in_f
+    return {"workload": name, "tflops": flops / (statistics.mean(ms) * 1e-3) / 1e12,
+            "ms": statistics.mean(ms), "ms_median": statistics.median(ms),
+            "rows": case.rows, "out_features": case.out_f, "in_features": case.in_f, "experts": case.E,
+            "l2": "flushed between launches (256 MB write)"}
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_wgrad_sample(case, n_sub: int, k_sub: int):
+    """Times the oracle (as it stands, single thread) on expert 0's tokens for an
+    n_sub x k_sub block of grad_w, including its quantization of that slice.
+    Returns (seconds, flops, description)."""
+    import oracle
+
+    off = case.expert_off
+    e = int(np.argmax(np.diff(off) > 0))
+    t0, t1 = int(off[e]), int(off[e + 1])
+    g = np.ascontiguousarray(case.g_bf16[t0:t1, :n_sub])
+    x = np.ascontiguousarray(case.x_bf16[t0:t1, :k_sub])
+    sub_off = [0, t1 - t0]
+    oracle.build()
+    start = time.perf_counter()
+    gq, gs = oracle.mxfp8_quantize(g, sub_off)
+    xq, xs = oracle.mxfp8_quantize(x, sub_off)
+    oracle.grouped_wgrad(gq, gs, xq, xs, sub_off)
+    sec = time.perf_counter() - start
+    flops = 2.0 * (t1 - t0) * n_sub * k_sub
+    return sec, flops, f"expert {e} ({t1 - t0} tokens), grad_w block {n_sub}x{k_sub}, quantize+wgrad, 1 thread"
+
+
+def cpu_baseline(case, target_s: float = 12.0):
+    sec, flops, _ = oracle_wgrad_sample(case, 128, 128)
+    scale = max(1.0, (target_s / max(sec, 1e-3)) ** 0.5)
+    n_sub = int(min(case.N, max(128, 128 * round(scale))))
+    k_sub = int(min(case.K, max(128, 128 * round(scale))))
+    sec, flops, desc = oracle_wgrad_sample(case, n_sub, k_sub)
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "seconds": sec}
+
+
+# --------------------------------------------------------------- dist glue
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend="nccl"):
+        import torch
+
+        if self.world > 1:
+            import torch.distributed as dist
+
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mgw", "reference"], default="mgw")
+    ap.add_argument("--workload", default="wgrad_8192",
+                    choices=["wgrad_tiny", "wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
+    ap.add_argument("--dgrad-workload", default="dgrad_4096", choices=["dgrad_4096", "moe_ffn_pair", "none"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    peaks = _peaks()
+    mxfp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+    metric = "MXFP8 grouped wgrad TFLOP/s"
+    d = Dist()
+
+    if args.impl == "reference":
+        if d.rank != 0:
+            return
+        case = wgrad_case(args.workload)
+        # bounded sample per step: expert 0's tokens, a 256 x 256 block of grad_w
+        for _ in range(args.warmup):
+            oracle_wgrad_sample(case, 128, 128)
+        secs, flops = [], 0.0
+        desc = ""
+        for _ in range(args.steps):
+            s, f, desc = oracle_wgrad_sample(case, 256, 256)
+            secs.append(s)
+            flops = f
+        v = flops * len(secs) / sum(secs) / 1e12
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * sum(secs) / len(secs), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "M": case.M, "N": case.N, "K": case.K,
+                           "experts": case.E, "sample": desc},
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    d.init("nccl")
+    torch.cuda.set_device(d.local_rank)
+    from moe_grouped_gemm_wgrad_gb300 import build as _build
+
+    _build.build()  # no-op when current
+    r = run_wgrad(args.workload, args.steps, args.warmup, d)
+    dg = None
+    if args.dgrad_workload != "none":
+        dg = run_dgrad(args.dgrad_workload, max(5, min(args.steps, 50)), max(3, args.warmup))
+    case = r["case"]
+    value = r["flops"] * d.world / (r["ms_per_step"] * 1e-3) / 1e12
+    wg_tflops = r["flops"] / (r["wgrad_ms"] * 1e-3) / 1e12
+    cpu = None
+    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case)
+    if d.rank == 0:
+        line = {
+            "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": d.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp8-e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+            "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "experts": case.E,
+                       "step": "mxfp8_quantize(g) + mxfp8_quantize(x) + grouped_wgrad_mxfp8",
+                       "l2": "inputs larger than L2 (bf16 g,x 2x134 MB; grad_w 1.07 GB per step)",
+                       "parallelism": f"replicas x{d.world} (independent workloads, no collective)"},
+            "roofline": {"bound": "tensor", "achieved": wg_tflops, "peak": mxfp8_peak,
+                         "unit": "TFLOP/s", "frac": wg_tflops / mxfp8_peak,
+                         "traffic": _traffic("grouped_wgrad_kernel", ["wgrad.cu", "ptx.cuh", "common.cuh"]),
+                         "kernel": "grouped_wgrad_kernel",
+                         "peak_note": f"2 x bf16 dense {peaks['bf16_tflops']} TFLOP/s ({peaks['source']}, burst)"},
+            "kernels_ms": {"mxfp8_quantize_g": r["quant_g_ms"], "mxfp8_quantize_x": r["quant_x_ms"],
+                           "grouped_wgrad": r["wgrad_ms"], "grouped_wgrad_median": r["wgrad_ms_median"]},
+            "quantize_hbm": {"achieved_gbs": r["quant_bytes"] / ((r["quant_g_ms"] + r["quant_x_ms"]) * 1e-3) / 1e9,
+                             "peak_gbs": peaks["hbm_gbs"]},
+            "e2e": {"value": r["flops"] * d.world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+            "cpu_baseline": cpu,
+        }
+        if dg is not None:
+            tf32_peak = peaks["bf16_tflops"] / 2.0  # nominal tf32 : bf16 dense ratio 1.1 : 2.25
+            dg["roofline"] = {"bound": "tensor", "tf32_work_tflops": 3 * dg["tflops"], "peak": tf32_peak,
+                              "unit": "TFLOP/s", "frac": 3 * dg["tflops"] / tf32_peak,
+                              "note": "3xTF32: three tf32 MMAs per fp32 product"}
+            line["dgrad"] = dg
+        print(json.dumps(line))
+    d.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * mgw -- grouped MoE backward GEMMs for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libmgw.so.  Every entry point takes plain device pointers, sizes and
+ * a CUDA stream handle; nothing here depends on PyTorch.  All device work is
+ * asynchronous on `stream` (a cudaStream_t passed as void*; NULL means the
+ * legacy default stream).  The library allocates no device memory: the caller
+ * owns every buffer.  Host-detectable argument errors return a negative status
+ * before anything is launched; data errors that only the device can see (an
+ * invalid expert_off array) are reported by OR-ing MGW_DEV_* bits into the
+ * caller's int status word, and the kernels then leave their outputs untouched.
+ * No entry point aborts, traps or blocks the host.
+ *
+ * Pages restated (cited by title and part):
+ *   wgrad page  "tinygrad/extra/thunder/amd/grouped_mxfp8_wgrad.cpp" -- the
+ *               grouped MXFP8 expert weight gradient kernel.
+ *   dgrad page  "oarust grouped_gemm_m_data_backward.slang" -- the grouped fp32
+ *               data-gradient compute shader.
+ *   post-attn page  vLLM "models/minimax_m3/amd/mono/kernels/post_attn" -- its
+ *               MXFP8 quantizer (mx8_scale / mx8_q) for the saturating clamp.
+ *   OCP "OFP8 Formats" v1.0 and "Microscaling Formats (MX)" v1.0.
+ */
+#ifndef MGW_H
+#define MGW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int mgw_status;
+
+/* Return codes. */
+#define MGW_OK 0
+#define MGW_ERR_INVALID_ARG (-1)  /* null pointer, negative size, E out of range */
+#define MGW_ERR_UNSUPPORTED (-2)  /* a size that is not a supported multiple */
+#define MGW_ERR_CAPACITY (-3)     /* Mcap too small or not a multiple of 128 */
+#define MGW_ERR_CUDA (-4)         /* a CUDA runtime/driver call or launch failed */
+#define MGW_ERR_ARCH (-5)         /* current device is not compute capability 10.3 */
+
+/* Bits OR-ed into *status_dev by the kernels (the caller zeroes it). */
+#define MGW_DEV_BAD_OFFSETS 1 /* expert_off[0] != 0, decreasing, or expert_off[E] != M/rows */
+#define MGW_DEV_TIMEOUT 2     /* an internal pipeline wait exceeded 1 s; outputs undefined */
+
+#define MGW_MAX_EXPERTS 1024
+
+/* Human-readable name of a return code (static string). */
+const char *mgw_status_string(mgw_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int mgw_version(void);
+
+/* ------------------------------------------------------------- layout helpers
+ * The quantized operands live on a padded token axis of length Mcap: expert e's
+ * tokens start at P[e] = sum_{e'<e} ceil128(expert_off[e'+1] - expert_off[e']),
+ * so every expert segment starts on a 128-token boundary and its tail up to the
+ * next boundary is zero.  Host-only helpers, no device work. */
+
+/* Smallest Mcap valid for any split of M tokens over E experts:
+ * ceil128(M + 127*E).  Returns 0 for negative M or E < 1. */
+size_t mgw_mxfp8_token_capacity(int M, int E);
+
+/* Bytes of the e8m0 scale buffer for C features on an Mcap token axis: C*Mcap/32. */
+size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap);
+
+/* --------------------------------------------------------------- quantize
+ * mgw_mxfp8_quantize -- MXFP8 quantization of one wgrad operand along the token
+ * (contraction) axis, transposed to token-contiguous rows.
+ *
+ * Defines the operands A = g^T and B = x^T of the wgrad page's kernel (its
+ * `gl<fp8e4m3, 1, 1, N, M>` / `gl<fp8e4m3, 1, 1, K, M>` declarations and the
+ * e8m0 scale tensors with four scales per 128 tokens).  For every feature c and
+ * every block of 32 consecutive tokens of one expert (blocks restart at each
+ * expert's first token and never mix experts):
+ *   amax = max |v| over the block's tokens,
+ *   scale = 2^s, s = clamp(floor(log2 amax) - 8, -127, 127)   (OCP MX rule;
+ *           amax == 0 gives s = -127),
+ *   q = e4m3(v / scale), rounded to nearest even, |q| saturated at 448 (the
+ *       post-attn page's mx8_q clamp).
+ *
+ * src_bf16   device, bf16 [M, C] row-major (token-major), read only.
+ * M          tokens, >= 0.  C: features, a positive multiple of 128.
+ * expert_off device int32 [E+1]: expert e owns tokens expert_off[e] ..
+ *            expert_off[e+1]-1; must be 0 = off[0] <= off[1] <= ... <= off[E] = M.
+ * E          experts, 1 .. MGW_MAX_EXPERTS.
+ * q_e4m3     device, uint8 [C, Mcap]: row c holds feature c's e4m3 bytes on the
+ *            padded token axis; every byte of the buffer is written (pads 0).
+ * scales_e8m0 device, mgw_mxfp8_scale_bytes(C, Mcap) bytes, every byte written
+ *            (pads 0), in tcgen05 scale-factor atoms: for feature c and padded
+ *            token t the byte is at
+ *              ((t/128) * (C/128) + c/128) * 512 + (c%32)*16 + ((c%128)/32)*4 + (t%128)/32.
+ * Mcap       padded token axis, multiple of 128, >= mgw_mxfp8_token_capacity(M, E).
+ * status_dev device int, nullable.  With NULL an invalid expert_off is not
+ *            reported (the kernel still writes nothing).
+ * Returns MGW_OK or a negative code; no work is launched on error.
+ */
+mgw_status mgw_mxfp8_quantize(const void *src_bf16, int M, int C, const int32_t *expert_off,
+                              int E, void *q_e4m3, void *scales_e8m0, size_t Mcap,
+                              int *status_dev, void *stream);
+
+/* ---------------------------------------------------------------- wgrad
+ * mgw_grouped_wgrad_mxfp8 -- grouped expert weight gradient
+ *   grad_w[e*N + n, k] = sum over tokens t of expert e of g[t, n] * x[t, k]
+ * from MXFP8 operands (each element times its block's e8m0 scale), accumulated
+ * in fp32 and stored as bf16 (round to nearest even).  This is the wgrad page's
+ * grouped_mxfp8_wgrad_kernel: per-expert token range from expert_off, scaled
+ * fp8 MMAs over 32-token scale blocks, experts stacked along the output rows,
+ * accumulators that start at zero so an expert without tokens gets zero rows.
+ *
+ * gq, gs     g quantized by mgw_mxfp8_quantize with C = N (same expert_off, Mcap).
+ * xq, xs     x quantized by mgw_mxfp8_quantize with C = K.
+ * expert_off device int32 [E+1], as for the quantizer; M = expert_off[E].
+ * N          grad_w rows per expert, a positive multiple of 128.
+ * K          grad_w columns, a positive multiple of 256.
+ * Mcap       the padded token axis both operands were quantized on.
+ * out_bf16   device, bf16 [E*N, K] row-major, fully written.
+ * status_dev device int, nullable (see MGW_DEV_*).
+ * Gradients accumulate over at most 2^24 tokens per expert without loss of
+ * fp32 integer-count exactness; inputs must be finite.
+ */
+mgw_status mgw_grouped_wgrad_mxfp8(const void *gq, const void *gs, const void *xq,
+                                   const void *xs, const int32_t *expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, void *out_bf16, int *status_dev,
+                                   void *stream);
+
+/* ---------------------------------------------------------------- dgrad
+ * mgw_grouped_dgrad_f32 -- grouped data gradient
+ *   dx[r, k] = sum_n dy[r, n] * W[e(r), n, k]
+ * where e(r) is the expert whose row range expert_off[e] <= r < expert_off[e+1]
+ * holds r (the dgrad page's expert_for_row; empty experts own no row).  fp32
+ * in and out, computed with 3xTF32 tensor-core products (hi*hi + hi*lo + lo*hi,
+ * Ootomo & Yokota 2022) and fp32 accumulation.  Row segments need not align to
+ * any tile.
+ *
+ * dy         device, fp32 [rows, out_f] row-major.
+ * W          device, fp32 [E, out_f, in_f] row-major (in_f contiguous), the dgrad
+ *            page's weight layout W[(e*out_f + n)*in_f + k].
+ * expert_off device int32 [E+1], 0 = off[0] <= ... <= off[E] = rows.
+ * rows >= 0; out_f a positive multiple of 32; in_f a positive multiple of 256.
+ * dx         device, fp32 [rows, in_f] row-major, fully written.
+ * status_dev device int, nullable.
+ */
+mgw_status mgw_grouped_dgrad_f32(const float *dy, const float *W, const int32_t *expert_off,
+                                 int E, int rows, int out_f, int in_f, float *dx,
+                                 int *status_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MGW_H */

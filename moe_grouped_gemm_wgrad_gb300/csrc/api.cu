@@ -1,0 +1,191 @@
+// C ABI of libmgw.so (declared in include/mgw.h): argument checks, TMA tensor
+// maps, device checks and kernel launches.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mgw.h"
+#include "kernels.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+// Checks that the current device is compute capability 10.3 and returns its SM count.
+mgw_status current_device(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MGW_ERR_CUDA;
+  static DeviceInfo cache[64];
+  static std::mutex mu;
+  if (dev < 0 || dev >= 64) return MGW_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MGW_ERR_CUDA;
+    if (major != 10 || minor != 3) return MGW_ERR_ARCH;
+    cache[dev].sms = sms;
+    cache[dev].ok = true;
+  }
+  *info = cache[dev];
+  return MGW_OK;
+}
+
+// 2-D tiled tensor map: `inner` contiguous elements per row, `outer` rows,
+// `pitch` bytes between rows.
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  std::memset(m, 0, sizeof(*m));
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mgw_status_string(mgw_status s) {
+  switch (s) {
+    case MGW_OK: return "ok";
+    case MGW_ERR_INVALID_ARG: return "invalid argument";
+    case MGW_ERR_UNSUPPORTED: return "unsupported size";
+    case MGW_ERR_CAPACITY: return "padded token capacity too small or not a multiple of 128";
+    case MGW_ERR_CUDA: return "CUDA error";
+    case MGW_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    default: return "unknown status";
+  }
+}
+
+int mgw_version(void) { return 100; }
+
+size_t mgw_mxfp8_token_capacity(int M, int E) {
+  if (M < 0 || E < 1) return 0;
+  const size_t need = static_cast<size_t>(M) + 127u * static_cast<size_t>(E);
+  return (need + 127u) / 128u * 128u;
+}
+
+size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap) {
+  if (C < 0) return 0;
+  return static_cast<size_t>(C) * Mcap / 32u;
+}
+
+mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t* expert_off,
+                              int E, void* q_e4m3, void* scales_e8m0, size_t Mcap,
+                              int* status_dev, void* stream) {
+  if (!expert_off || !q_e4m3 || !scales_e8m0 || (M > 0 && !src_bf16)) return MGW_ERR_INVALID_ARG;
+  if (M < 0 || C <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
+  if (C % 128 != 0) return MGW_ERR_UNSUPPORTED;
+  if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if ((src_bf16 && !aligned16(src_bf16)) || !aligned16(q_e4m3) || !aligned16(scales_e8m0))
+    return MGW_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  mgw_status st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  const cudaError_t err = mgw::launch_mxfp8_quantize(
+      src_bf16, M, C, expert_off, E, q_e4m3, scales_e8m0, static_cast<long long>(Mcap),
+      status_dev, dev.sms, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* xq,
+                                   const void* xs, const int32_t* expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, void* out_bf16, int* status_dev,
+                                   void* stream) {
+  if (!gq || !gs || !xq || !xs || !expert_off || !out_bf16) return MGW_ERR_INVALID_ARG;
+  if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 256 != 0) return MGW_ERR_UNSUPPORTED;
+  if (static_cast<long long>(E) * N > (1ll << 31)) return MGW_ERR_UNSUPPORTED;
+  if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if (!aligned16(gq) || !aligned16(xq) || !aligned16(gs) || !aligned16(xs) || !aligned16(out_bf16))
+    return MGW_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  mgw_status st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  mgw::WgradArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!make_map_2d(&a.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, Mcap, N, Mcap, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128, 256,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_bf16, K,
+                   static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return MGW_ERR_CUDA;
+  a.gs = static_cast<const uint8_t*>(gs);
+  a.xs = static_cast<const uint8_t*>(xs);
+  a.expert_off = expert_off;
+  a.E = E;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.status = status_dev;
+  const cudaError_t err = mgw::launch_grouped_wgrad(a, dev.sms, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t* expert_off,
+                                 int E, int rows, int out_f, int in_f, float* dx,
+                                 int* status_dev, void* stream) {
+  if (!W || !expert_off || (rows > 0 && (!dy || !dx))) return MGW_ERR_INVALID_ARG;
+  if (rows < 0 || out_f <= 0 || in_f <= 0 || E < 1 || E > MGW_MAX_EXPERTS)
+    return MGW_ERR_INVALID_ARG;
+  if (out_f % 32 != 0 || in_f % 256 != 0) return MGW_ERR_UNSUPPORTED;
+  if ((dy && !aligned16(dy)) || !aligned16(W) || (dx && !aligned16(dx)))
+    return MGW_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  mgw_status st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  mgw::DgradArgs a;
+  a.dy = dy;
+  a.W = W;
+  a.expert_off = expert_off;
+  a.dx = dx;
+  a.E = E;
+  a.rows = rows;
+  a.out_f = out_f;
+  a.in_f = in_f;
+  a.status = status_dev;
+  const cudaError_t err = mgw::launch_grouped_dgrad(a, dev.sms, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mgw {
+
+constexpr int kMaxExperts = 1024;
+
+size_t quantize_smem_bytes(int E);
+cudaError_t launch_mxfp8_quantize(const void* src, int M, int C, const int32_t* expert_off, int E,
+                                  void* q, void* sc, long long Mcap, int* status, int num_sms,
+                                  cudaStream_t stream);
+
+struct WgradArgs {
+  CUtensorMap tm_a;    // g^T e4m3 [N, Mcap], box 128 tokens x 128 rows, 128B swizzle
+  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x 256 rows, 128B swizzle
+  CUtensorMap tm_out;  // grad_w bf16 [E*N, K], box 64 cols x 128 rows, 128B swizzle
+  const uint8_t* gs;   // g scale atoms
+  const uint8_t* xs;   // x scale atoms
+  const int32_t* expert_off;
+  int E, M, N, K;
+  int* status;
+};
+cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream);
+
+struct DgradArgs {
+  const float* dy;
+  const float* W;
+  const int32_t* expert_off;
+  float* dx;
+  int E, rows, out_f, in_f;
+  int* status;
+};
+cudaError_t launch_grouped_dgrad(const DgradArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace mgw

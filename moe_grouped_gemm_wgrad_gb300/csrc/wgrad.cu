@@ -1,0 +1,320 @@
+// Grouped MXFP8 expert weight gradient on tcgen05 tensor cores.
+//
+//   grad_w[e*N + n, k] = sum_{t in expert e} g[t, n] * x[t, k]
+//
+// Work item = (expert, 128-row N tile, 256-column K tile); one item's output tile
+// is a 128 x 256 fp32 accumulator in TMEM (256 columns).  A persistent grid of one
+// CTA per SM walks the items in a static stride, experts ordered by descending
+// token count so the largest experts are spread first (LPT); experts with no
+// tokens become store-only items that write zero rows.
+//
+// Roles (320 threads):
+//   warp 0      TMA producer: per 128-token chunk, g^T tile 128x128 B, x^T tile
+//               256x128 B (both 128B-swizzled) and the two e8m0 scale-factor atom
+//               sets (512 B + 1 KB) into a 3-stage shared-memory ring.
+//   warp 1      MMA issuer: copies the chunk's scale atoms to TMEM (tcgen05.cp,
+//               32x128b.warpx4) and issues one block-scaled
+//               tcgen05.mma.kind::mxf8f6f4 (M=128, N=256, K=32) per 32-token block
+//               that holds tokens, then commits the stage back to the producer.
+//   warps 2-9   epilogue: drain the accumulator (each warp: its TMEM lane quarter,
+//               one 128-column half) into registers, release TMEM at once so the
+//               next item's MMAs start, then round to bf16, stage in 128B-swizzled
+//               shared memory and TMA-store four 64-column boxes.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mgw {
+namespace {
+
+constexpr int BM = 128;  // grad_w rows per tile (MMA M)
+constexpr int BN = 256;  // grad_w cols per tile (MMA N)
+constexpr int BT = 128;  // tokens per pipeline stage (four 32-token scale blocks)
+constexpr int kStages = 3;
+constexpr int kABytes = BM * BT;                 // 16 KB
+constexpr int kBBytes = BN * BT;                 // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB, 1024-aligned
+constexpr int kSfStage = 512 + 1024;             // SFA atom + two SFB atoms
+constexpr int kOutBytes = BM * BN * 2;           // bf16 staging, four 16 KB boxes
+constexpr int kOffOut = kStages * kStageBytes;
+constexpr int kOffSf = kOffOut + kOutBytes;
+constexpr int kOffBar = kOffSf + kStages * kSfStage;
+constexpr int kNumBars = 2 * kStages + 3;        // full[], empty[], acc_full, acc_empty, done
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kOffTable = kOffMisc + 16;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;  // scale slots: 16 TMEM columns per stage
+
+__host__ __device__ constexpr size_t wgrad_smem_bytes(int E) {
+  return static_cast<size_t>(kOffTable) + sizeof(int) * (3 * static_cast<size_t>(E) + 2) + 1024;
+}
+static_assert(wgrad_smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
+  const __nv_bfloat162 v =
+      __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Waits without honouring the abort flag (used to drain in-flight async work).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  int never = 0;
+  (void)mbar_wait(bar, parity, &never);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid_constant__ WgradArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int E = args.E, N = args.N, K = args.K;
+  int* s_misc = reinterpret_cast<int*>(smem + kOffMisc);  // [0] tmem base [1] abort [2] flag
+  int* s_off = reinterpret_cast<int*>(smem + kOffTable);
+  int* s_pad = s_off + (E + 1);
+  int* s_order = s_pad + (E + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_misc[1]);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const uint32_t lane = lane_id();
+
+  if (tid == 0) s_misc[1] = 0;
+  if (!load_offsets(args.expert_off, E, args.M, s_off, s_pad, &s_misc[2], args.status)) return;
+
+  // LPT order: experts by descending token count, ties by index.
+  for (int e = tid; e < E; e += kThreads) {
+    const int ce = s_off[e + 1] - s_off[e];
+    int rank = 0;
+    for (int j = 0; j < E; ++j) {
+      const int cj = s_off[j + 1] - s_off[j];
+      rank += (cj > ce) || (cj == ce && j < e);
+    }
+    s_order[rank] = e;
+  }
+  const uint32_t bar0 = sbase + kOffBar;
+  auto bar_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t bar_acc_full = bar0 + 8u * (2 * kStages);
+  const uint32_t bar_acc_empty = bar0 + 8u * (2 * kStages + 1);
+  const uint32_t bar_done = bar0 + 8u * (2 * kStages + 2);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, kEpiWarps);
+    mbar_init(bar_done, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&args.tm_a);
+    tma_prefetch_desc(&args.tm_b);
+    tma_prefetch_desc(&args.tm_out);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
+
+  const int tiles_n = N / BM, tiles_k = K / BN;
+  const long long per_expert = static_cast<long long>(tiles_n) * tiles_k;
+  const long long total = per_expert * E;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int pending[kStages];
+      uint32_t pending_phase[kStages];
+      for (int s = 0; s < kStages; ++s) pending[s] = 0, pending_phase[s] = 0;
+      bool ok = true;
+      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const int e = s_order[it / per_expert];
+        const int tile = static_cast<int>(it % per_expert);
+        const int nt = tile / tiles_k, kt = tile % tiles_k;
+        const int cnt = s_off[e + 1] - s_off[e];
+        if (cnt == 0) continue;
+        const int nch = (cnt + BT - 1) / BT;
+        const int ch0 = s_pad[e] / BT;
+        for (int c = 0; c < nch; ++c) {
+          if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full(stage);
+          mbar_arrive_expect_tx(fb, kStageBytes + kSfStage);
+          const uint32_t sa = sbase + stage * kStageBytes;
+          const int tok = (ch0 + c) * BT;
+          tma_load_2d(sa, &args.tm_a, tok, nt * BM, fb);
+          tma_load_2d(sa + kABytes, &args.tm_b, tok, kt * BN, fb);
+          const uint32_t ssf = sbase + kOffSf + stage * kSfStage;
+          bulk_load(ssf, args.gs + (static_cast<size_t>(ch0 + c) * tiles_n + nt) * 512, 512, fb);
+          bulk_load(ssf + 512,
+                    args.xs + (static_cast<size_t>(ch0 + c) * (K / 128) + 2 * kt) * 512, 1024, fb);
+          pending[stage] = 1;
+          pending_phase[stage] = phase;
+          if (++stage == kStages) stage = 0, phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        if (args.status) atomicOr(args.status, kDevTimeout);
+      }
+      // Never leave the CTA with copies still landing in shared memory.
+      for (int s = 0; s < kStages; ++s)
+        if (pending[s]) mbar_wait_drain(bar_full(s), pending_phase[s]);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const int e = s_order[it / per_expert];
+        const int cnt = s_off[e + 1] - s_off[e];
+        if (cnt == 0) continue;
+        if (!mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int nch = (cnt + BT - 1) / BT;
+        for (int c = 0; c < nch; ++c) {
+          if (!mbar_wait(bar_full(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ssf = sbase + kOffSf + stage * kSfStage;
+          const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
+          // Scale atoms: 32 rows x 16 B, 8-row core matrices 128 B apart.
+          tmem_cp_32x128b_warpx4(tsf, make_sdesc(ssf, 0, 128, 0));
+          tmem_cp_32x128b_warpx4(tsf + 8, make_sdesc(ssf + 512, 0, 128, 0));
+          tmem_cp_32x128b_warpx4(tsf + 12, make_sdesc(ssf + 1024, 0, 128, 0));
+          const int rem = cnt - c * BT;
+          const int nkb = rem >= BT ? 4 : (rem + 31) / 32;
+          const uint32_t sa = sbase + stage * kStageBytes;
+          for (int kb = 0; kb < nkb; ++kb) {
+            mma_mxf8_block32(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
+                             sdesc_kmajor_sw128(sa + kABytes + 32 * kb),
+                             idesc_mxf8_e4m3(BM, BN, kb, kb), tsf, tsf + 8, (c | kb) != 0);
+          }
+          mma_commit(bar_empty(stage));
+          if (++stage == kStages) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        mma_commit(bar_acc_full);
+        acc_phase ^= 1u;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        if (args.status) atomicOr(args.status, kDevTimeout);
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      mma_commit(bar_done);
+      mbar_wait_drain(bar_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int half = ew >> 2;      // output columns [128*half, 128*half + 128)
+    const int row = quarter * 32 + static_cast<int>(lane);
+    const bool leader = (ew == 0 && lane == 0);
+    uint32_t acc_phase = 0;
+    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+      const int e = s_order[it / per_expert];
+      const int tile = static_cast<int>(it % per_expert);
+      const int nt = tile / tiles_k, kt = tile % tiles_k;
+      const int cnt = s_off[e + 1] - s_off[e];
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) pk[j] = 0u;
+      if (cnt > 0 && !*abort_flag) {
+        if (mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
+          tc_fence_after();
+          uint32_t r[128];
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 128u * half;
+          tmem_ld_32x32b_x32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_ld_32x32b_x32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+          tmem_ld_32x32b_x32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acc_empty);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
+        } else {
+          *abort_flag = 1;
+          if (lane == 0 && args.status) atomicOr(args.status, kDevTimeout);
+        }
+        acc_phase ^= 1u;
+      }
+      // The previous item's TMA store must have finished reading the staging tile.
+      if (leader) bulk_wait_read0();
+      named_bar_sync(1, kEpiWarps * 32);
+      const uint32_t stage_base = sbase + kOffOut;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int box = half * 2 + (jj >> 3);
+        const int chunk = jj & 7;
+        const uint32_t addr = stage_base + box * 16384 + row * 128 + ((chunk ^ (row & 7)) << 4);
+        st_shared_v4(addr, pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+      }
+      fence_async_smem();
+      named_bar_sync(1, kEpiWarps * 32);
+      if (leader && !*abort_flag) {
+        const int orow = e * N + nt * BM;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          tma_store_2d(&args.tm_out, kt * BN + 64 * b, orow, stage_base + b * 16384);
+        bulk_commit();
+      }
+    }
+    if (leader) bulk_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream) {
+  static thread_local int attr_set_device = -1;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (attr_set_device != dev) {
+    err = cudaFuncSetAttribute(grouped_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(wgrad_smem_bytes(kMaxExperts)));
+    if (err != cudaSuccess) return err;
+    attr_set_device = dev;
+  }
+  const long long total = static_cast<long long>(a.N / BM) * (a.K / BN) * a.E;
+  long long grid = num_sms;
+  if (grid > total) grid = total;
+  if (grid < 1) grid = 1;
+  grouped_wgrad_kernel<<<static_cast<unsigned>(grid), kThreads, wgrad_smem_bytes(a.E), stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mgw

@@ -1,0 +1,152 @@
+"""Thin ctypes binding of libmgw.so (C ABI in include/mgw.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.  If the
+library is missing or fails to load, every call raises :class:`MgwError`;
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmgw.so")
+
+MGW_OK = 0
+MGW_DEV_BAD_OFFSETS = 1
+MGW_DEV_TIMEOUT = 2
+MAX_EXPERTS = 1024
+
+EXPORTS = (
+    "mgw_status_string", "mgw_version", "mgw_mxfp8_token_capacity", "mgw_mxfp8_scale_bytes",
+    "mgw_mxfp8_quantize", "mgw_grouped_wgrad_mxfp8", "mgw_grouped_dgrad_f32",
+)
+
+
+class MgwError(RuntimeError):
+    pass
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libmgw.so (built in-tree by ``moe_grouped_gemm_wgrad_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise MgwError(f"{LIB_PATH} is not built; run `python -m moe_grouped_gemm_wgrad_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.mgw_status_string.argtypes = [I]
+        lib.mgw_status_string.restype = ctypes.c_char_p
+        lib.mgw_version.argtypes = []
+        lib.mgw_version.restype = I
+        lib.mgw_mxfp8_token_capacity.argtypes = [I, I]
+        lib.mgw_mxfp8_token_capacity.restype = SZ
+        lib.mgw_mxfp8_scale_bytes.argtypes = [I, SZ]
+        lib.mgw_mxfp8_scale_bytes.restype = SZ
+        lib.mgw_mxfp8_quantize.argtypes = [P, I, I, P, I, P, P, SZ, P, P]
+        lib.mgw_mxfp8_quantize.restype = I
+        lib.mgw_grouped_wgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
+        lib.mgw_grouped_wgrad_mxfp8.restype = I
+        lib.mgw_grouped_dgrad_f32.argtypes = [P, P, P, I, I, I, I, P, P, P]
+        lib.mgw_grouped_dgrad_f32.restype = I
+        _lib = lib
+        return lib
+
+
+def _check(st: int, what: str) -> None:
+    if st != MGW_OK:
+        msg = load().mgw_status_string(st).decode()
+        raise MgwError(f"{what}: {msg} (status {st})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_tensor(t: torch.Tensor, dtype, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise MgwError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MgwError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MgwError(f"{name} must be contiguous")
+
+
+def token_capacity(M: int, E: int) -> int:
+    """Padded token axis length that fits any split of M tokens over E experts."""
+    return int(load().mgw_mxfp8_token_capacity(int(M), int(E)))
+
+
+def scale_bytes(C: int, Mcap: int) -> int:
+    return int(load().mgw_mxfp8_scale_bytes(int(C), int(Mcap)))
+
+
+def mxfp8_quantize(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int | None = None,
+                   q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                   status: torch.Tensor | None = None, stream=None):
+    """MXFP8-quantize bf16 ``src`` [M, C] along tokens -> (q uint8 [C, Mcap], scales uint8)."""
+    _dev_tensor(src, torch.bfloat16, "src")
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    M, C = src.shape
+    E = expert_off.numel() - 1
+    if Mcap is None:
+        Mcap = token_capacity(M, E)
+    if q is None:
+        q = torch.empty((C, Mcap), dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
+    st = load().mgw_mxfp8_quantize(_ptr(src), M, C, _ptr(expert_off), E, _ptr(q), _ptr(scales),
+                                   Mcap, _ptr(status), _stream(stream))
+    _check(st, "mgw_mxfp8_quantize")
+    return q, scales
+
+
+def grouped_wgrad_mxfp8(gq: torch.Tensor, gs: torch.Tensor, xq: torch.Tensor, xs: torch.Tensor,
+                        expert_off: torch.Tensor, M: int, out: torch.Tensor | None = None,
+                        status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """grad_w [E*N, K] bf16 from quantized g^T (N rows) and x^T (K rows)."""
+    for t, n in ((gq, "gq"), (gs, "gs"), (xq, "xq"), (xs, "xs")):
+        _dev_tensor(t, torch.uint8, n)
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    N, Mcap = gq.shape
+    K = xq.shape[0]
+    E = expert_off.numel() - 1
+    if out is None:
+        out = torch.empty((E * N, K), dtype=torch.bfloat16, device=gq.device)
+    st = load().mgw_grouped_wgrad_mxfp8(_ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off),
+                                        E, int(M), N, K, Mcap, _ptr(out), _ptr(status),
+                                        _stream(stream))
+    _check(st, "mgw_grouped_wgrad_mxfp8")
+    return out
+
+
+def grouped_dgrad_f32(dy: torch.Tensor, W: torch.Tensor, expert_off: torch.Tensor,
+                      out: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """dx [rows, in_f] fp32 = dy[r] . W[e(r)] per row's expert."""
+    _dev_tensor(dy, torch.float32, "dy")
+    _dev_tensor(W, torch.float32, "W")
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    rows, out_f = dy.shape
+    E, _, in_f = W.shape
+    if out is None:
+        out = torch.empty((rows, in_f), dtype=torch.float32, device=dy.device)
+    st = load().mgw_grouped_dgrad_f32(_ptr(dy), _ptr(W), _ptr(expert_off), E, rows, out_f, in_f,
+                                      _ptr(out), _ptr(status), _stream(stream))
+    _check(st, "mgw_grouped_dgrad_f32")
+    return out

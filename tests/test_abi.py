@@ -1,0 +1,66 @@
+"""The C ABI on the host: the library and the header agree, helpers compute the
+documented sizes, and argument errors return codes before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_grouped_gemm_wgrad_gb300 import build, mgw
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mgw.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "mgw.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mgw_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    declared = _declared_functions()
+    assert set(declared) == set(mgw.EXPORTS), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_host_helpers(lib):
+    assert lib.mgw_version() >= 100
+    assert lib.mgw_mxfp8_token_capacity(256, 2) == 512
+    assert lib.mgw_mxfp8_token_capacity(8192, 8) == 9216
+    assert lib.mgw_mxfp8_token_capacity(65536, 64) == 73728
+    assert lib.mgw_mxfp8_token_capacity(-1, 2) == 0
+    assert lib.mgw_mxfp8_scale_bytes(256, 512) == 256 * 512 // 32
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.mgw_status_string(code)
+
+
+def test_argument_errors_before_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: validation fails first
+    # null pointers
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, None, 1, fake, fake, 256, None, None) == -1
+    # C not a multiple of 128
+    assert lib.mgw_mxfp8_quantize(fake, 4, 96, fake, 1, fake, fake, 256, None, None) == -2
+    # Mcap too small / not a multiple of 128
+    assert lib.mgw_mxfp8_quantize(fake, 300, 128, fake, 2, fake, fake, 384, None, None) == -3
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1, fake, fake, 200, None, None) == -3
+    # E out of range
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 0, fake, fake, 256, None, None) == -1
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1025, fake, fake, 1 << 20, None, None) == -1
+    # wgrad: K not a multiple of 256, N not a multiple of 128
+    assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 64, 256, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_wgrad_mxfp8(None, fake, fake, fake, fake, 1, 4, 128, 256, 256, fake, None, None) == -1
+    # misaligned pointer
+    assert lib.mgw_grouped_wgrad_mxfp8(P(0x1001), fake, fake, fake, fake, 1, 4, 128, 256, 256, fake, None, None) == -1
+    # dgrad: in_f not a multiple of 256, out_f not a multiple of 32
+    assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1, 4, 32, 128, fake, None, None) == -2
+    assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1, 4, 48, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_dgrad_f32(fake, None, fake, 1, 4, 32, 256, fake, None, None) == -1

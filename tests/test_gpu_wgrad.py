@@ -1,0 +1,129 @@
+"""Grouped MXFP8 wgrad on the GPU against the fp64 oracle.
+
+Tolerance (from the workload definition): |gpu - ref| <= 8e-3 |ref| + 1e-3 rms(ref),
+with ref the unrounded fp64 value; the bf16 output alone contributes up to 2^-9 |ref|.
+Rows of experts without tokens must be exactly zero.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_gemm_wgrad_gb300 import mgw, synth
+from helpers import bf16_to_f64, dev_bf16, dev_i32, wgrad_tol
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_wgrad(case, Mcap=None):
+    off = dev_i32(case.expert_off)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if Mcap is None:
+        Mcap = mgw.token_capacity(case.M, case.E)
+    if case.M > 0:
+        g, x = dev_bf16(case.g_bf16), dev_bf16(case.x_bf16)
+    else:
+        g = torch.empty((0, case.N), dtype=torch.bfloat16, device="cuda")
+        x = torch.empty((0, case.K), dtype=torch.bfloat16, device="cuda")
+    gq, gs = mgw.mxfp8_quantize(g, off, Mcap=Mcap, status=status)
+    xq, xs = mgw.mxfp8_quantize(x, off, Mcap=Mcap, status=status)
+    out = torch.full((case.E * case.N, case.K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, case.M, out=out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, int(status.item())
+    return out
+
+
+def _oracle_operands(case, Mcap=None):
+    gq, gs = oracle.mxfp8_quantize(case.g_bf16, case.expert_off, Mcap)
+    xq, xs = oracle.mxfp8_quantize(case.x_bf16, case.expert_off, Mcap)
+    return gq, gs, xq, xs
+
+
+def _check_full(case):
+    out = bf16_to_f64(_gpu_wgrad(case))
+    ref = oracle.grouped_wgrad(*_oracle_operands(case), case.expert_off)
+    err = np.abs(out - ref)
+    tol = wgrad_tol(ref)
+    bad = np.argwhere(~(err <= tol))
+    assert bad.size == 0, (f"{len(bad)} of {ref.size} outside tolerance; first {bad[:5].tolist()} "
+                           f"got {out[tuple(bad[0])]} ref {ref[tuple(bad[0])]}")
+    counts = np.diff(case.expert_off)
+    for e in np.nonzero(counts == 0)[0]:
+        assert not out[e * case.N:(e + 1) * case.N].any()
+
+
+CASES = [
+    ("tiny", lambda: synth.wgrad_tiny()),
+    ("ragged_multi_tile", lambda: synth.wgrad_random(463, 256, 512, [0, 1, 129, 300, 33], seed=21)),
+    ("single_expert", lambda: synth.wgrad_random(200, 128, 256, [200], seed=22)),
+    ("empty_first_last", lambda: synth.wgrad_random(64, 128, 256, [0, 64, 0], seed=23)),
+    ("block_edges", lambda: synth.wgrad_random(481, 128, 256, [31, 32, 33, 127, 129, 128, 1], seed=24)),
+    ("outliers", lambda: synth.wgrad_random(384, 256, 256, [256, 0, 128], seed=25, outlier_frac=0.01)),
+    ("many_experts", lambda: synth.wgrad_random(
+        int(np.random.default_rng(26).integers(0, 40, 160).sum()), 128, 256,
+        np.random.default_rng(26).integers(0, 40, 160), seed=26)),
+]
+
+
+@pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
+def test_wgrad_matches_oracle(name, make):
+    _check_full(make())
+
+
+def test_wgrad_no_tokens_gives_zero():
+    case = synth.wgrad_random(0, 128, 256, [0, 0, 0], seed=1)
+    out = _gpu_wgrad(case)
+    assert not bool(out.float().abs().sum())
+
+
+def _check_sampled(case, n_samples=3000, seed=0):
+    out = _gpu_wgrad(case)
+    ops = _oracle_operands(case)
+    counts = np.diff(case.expert_off)
+    rng = np.random.default_rng(seed)
+    nz = np.nonzero(counts > 0)[0]
+    # samples weighted towards the tile edges and the last expert rows
+    es = rng.choice(nz, n_samples)
+    ns = rng.integers(0, case.N, n_samples)
+    ks = rng.integers(0, case.K, n_samples)
+    ns[:200] = rng.choice([0, 127, 128, case.N - 1], 200)
+    ks[:200] = rng.choice([0, 255, 256 % case.K, case.K - 1], 200)
+    ref = np.array([oracle.grouped_wgrad_element(*ops, case.expert_off, int(e), int(n), int(k))
+                    for e, n, k in zip(es, ns, ks)])
+    got = bf16_to_f64(out[torch.as_tensor(es * case.N + ns, device="cuda"), torch.as_tensor(ks, device="cuda")])
+    tol = wgrad_tol(ref)
+    bad = np.nonzero(~(np.abs(got - ref) <= tol))[0]
+    assert bad.size == 0, [(int(es[i]), int(ns[i]), int(ks[i]), got[i], ref[i]) for i in bad[:5]]
+    # rows of empty experts are exactly zero; all other rows are finite
+    full = out.view(case.E, case.N, case.K)
+    empty = torch.as_tensor(np.nonzero(counts == 0)[0], device="cuda")
+    if empty.numel():
+        assert not bool(full[empty].float().abs().amax())
+    assert bool(torch.isfinite(out.float()).all())
+
+
+def test_wgrad_more_items_than_sms_sampled():
+    _check_sampled(synth.wgrad_random(800, 2048, 2048, [300, 0, 500], seed=27))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
+def test_wgrad_full_size_sampled(name):
+    case = synth.moe_ffn_pair()[0] if name == "moe_ffn_pair" else getattr(synth, name)()
+    _check_sampled(case)
+
+
+def test_wgrad_bad_offsets_reported_and_output_untouched():
+    case = synth.wgrad_random(64, 128, 256, [32, 32], seed=1)
+    Mcap = mgw.token_capacity(64, 2)
+    gq = torch.zeros((128, Mcap), dtype=torch.uint8, device="cuda")
+    xq = torch.zeros((256, Mcap), dtype=torch.uint8, device="cuda")
+    gs = torch.zeros((mgw.scale_bytes(128, Mcap),), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((mgw.scale_bytes(256, Mcap),), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((256, 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, dev_i32([0, 40, 30]), 64, out=out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & mgw.MGW_DEV_BAD_OFFSETS
+    assert bool((out == 3.0).all())
