@@ -61,55 +61,64 @@ def _traffic(kernel: str, src_files) -> float | None:
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks / throttle reasons, sampled every 50 ms; only the samples whose
+    timestamps fall inside the timed window are summarised."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int, path: str | None):
         self.proc = None
         self.path = path
-        self.gpu = gpu_index
+        self.window = None
         if path is None:
             return
         try:
             self.fh = open(path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(1.0)  # let the sampler come up before the timed region
         except Exception:
             self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.15)
+        time.sleep(0.2)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx = max(mx, float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        if not sm:
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        use = inside if inside else rows
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted({n for r in use for n, v in zip(self.NAMES, r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "power_w_median": statistics.median(r[3] for r in use), "reasons": reasons,
+                "samples": len(use), "samples_in_timed_window": len(inside)}
 
 
 # ----------------------------------------------------------------- workloads
@@ -158,6 +167,8 @@ def run_wgrad(name, steps, warmup, dist_ctx):
         mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)
         mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
 
+    clocks = ClockSampler(dist_ctx.local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_r{dist_ctx.rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -165,10 +176,9 @@ def run_wgrad(name, steps, warmup, dist_ctx):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     dist_ctx.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(dist_ctx.local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_r{dist_ctx.rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    host_t0 = time.time()
     t_start.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
@@ -180,6 +190,7 @@ def run_wgrad(name, steps, warmup, dist_ctx):
         ev[i][3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(host_t0, time.time())
     dist_ctx.barrier()
     clk = clocks.stop()
     total_ms = dist_ctx.max(t_start.elapsed_time(t_end))
@@ -333,7 +344,7 @@ class Dist:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mgw", "reference"], default="mgw")
     ap.add_argument("--workload", default="wgrad_8192",

@@ -11,15 +11,16 @@
 // Roles (320 threads):
 //   warp 0      TMA producer: per 128-token chunk, g^T tile 128x128 B, x^T tile
 //               256x128 B (both 128B-swizzled) and the two e8m0 scale-factor atom
-//               sets (512 B + 1 KB) into a 3-stage shared-memory ring.
+//               sets (512 B + 1 KB) into a 4-stage shared-memory ring.
 //   warp 1      MMA issuer: copies the chunk's scale atoms to TMEM (tcgen05.cp,
 //               32x128b.warpx4) and issues one block-scaled
 //               tcgen05.mma.kind::mxf8f6f4 (M=128, N=256, K=32) per 32-token block
 //               that holds tokens, then commits the stage back to the producer.
 //   warps 2-9   epilogue: drain the accumulator (each warp: its TMEM lane quarter,
 //               one 128-column half) into registers, release TMEM at once so the
-//               next item's MMAs start, then round to bf16, stage in 128B-swizzled
-//               shared memory and TMA-store four 64-column boxes.
+//               next item's MMAs start, then round to bf16 and TMA-store the tile as
+//               four 128 x 64 boxes through one 16 KB 128B-swizzled staging tile
+//               (one box at a time, so the ring can hold four 48 KB stages).
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -33,12 +34,12 @@ namespace {
 constexpr int BM = 128;  // grad_w rows per tile (MMA M)
 constexpr int BN = 256;  // grad_w cols per tile (MMA N)
 constexpr int BT = 128;  // tokens per pipeline stage (four 32-token scale blocks)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kABytes = BM * BT;                 // 16 KB
 constexpr int kBBytes = BN * BT;                 // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB, 1024-aligned
 constexpr int kSfStage = 512 + 1024;             // SFA atom + two SFB atoms
-constexpr int kOutBytes = BM * BN * 2;           // bf16 staging, four 16 KB boxes
+constexpr int kOutBytes = BM * 64 * 2;           // bf16 staging: one 128 x 64 box (16 KB)
 constexpr int kOffOut = kStages * kStageBytes;
 constexpr int kOffSf = kOffOut + kOutBytes;
 constexpr int kOffBar = kOffSf + kStages * kSfStage;
@@ -50,8 +51,10 @@ constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;  // scale slots: 16 TMEM columns per stage
 
+// Tables: expert_off and padded starts (int, E+1 each), LPT order (uint16, E).
 __host__ __device__ constexpr size_t wgrad_smem_bytes(int E) {
-  return static_cast<size_t>(kOffTable) + sizeof(int) * (3 * static_cast<size_t>(E) + 2) + 1024;
+  return static_cast<size_t>(kOffTable) + sizeof(int) * (2 * static_cast<size_t>(E) + 2) +
+         sizeof(uint16_t) * static_cast<size_t>(E) + 1024;
 }
 static_assert(wgrad_smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
 
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
   int* s_misc = reinterpret_cast<int*>(smem + kOffMisc);  // [0] tmem base [1] abort [2] flag
   int* s_off = reinterpret_cast<int*>(smem + kOffTable);
   int* s_pad = s_off + (E + 1);
-  int* s_order = s_pad + (E + 1);
+  uint16_t* s_order = reinterpret_cast<uint16_t*>(s_pad + (E + 1));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_misc[1]);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       const int cj = s_off[j + 1] - s_off[j];
       rank += (cj > ce) || (cj == ce && j < e);
     }
-    s_order[rank] = e;
+    s_order[rank] = static_cast<uint16_t>(e);
   }
   const uint32_t bar0 = sbase + kOffBar;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
@@ -266,25 +269,28 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
         }
         acc_phase ^= 1u;
       }
-      // The previous item's TMA store must have finished reading the staging tile.
-      if (leader) bulk_wait_read0();
-      named_bar_sync(1, kEpiWarps * 32);
+      // Four 128 x 64 boxes go out through one 16 KB staging tile, one after another:
+      // the warps of the box's column half write it (128B swizzle), one thread stores it.
       const uint32_t stage_base = sbase + kOffOut;
+      const int orow = e * N + nt * BM;
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int box = half * 2 + (jj >> 3);
-        const int chunk = jj & 7;
-        const uint32_t addr = stage_base + box * 16384 + row * 128 + ((chunk ^ (row & 7)) << 4);
-        st_shared_v4(addr, pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
-      }
-      fence_async_smem();
-      named_bar_sync(1, kEpiWarps * 32);
-      if (leader && !*abort_flag) {
-        const int orow = e * N + nt * BM;
+      for (int b = 0; b < 4; ++b) {
+        if (leader) bulk_wait_read0();  // the previous box has left the staging tile
+        named_bar_sync(1, kEpiWarps * 32);
+        if ((b >> 1) == half) {
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          tma_store_2d(&args.tm_out, kt * BN + 64 * b, orow, stage_base + b * 16384);
-        bulk_commit();
+          for (int chunk = 0; chunk < 8; ++chunk) {
+            const int jj = (b & 1) * 8 + chunk;
+            const uint32_t addr = stage_base + row * 128 + ((chunk ^ (row & 7)) << 4);
+            st_shared_v4(addr, pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+          }
+          fence_async_smem();
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (leader && !*abort_flag) {
+          tma_store_2d(&args.tm_out, kt * BN + 64 * b, orow, stage_base);
+          bulk_commit();
+        }
       }
     }
     if (leader) bulk_wait0();
