@@ -119,8 +119,14 @@ mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t*
   DeviceInfo dev;
   mgw_status st = current_device(&dev);
   if (st != MGW_OK) return st;
+  // With M == 0 no tile is ever loaded; the map then only needs a valid address.
+  CUtensorMap tm_src;
+  if (!make_map_2d(&tm_src, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M > 0 ? src_bf16 : q_e4m3, C,
+                   M > 0 ? static_cast<uint64_t>(M) : 1, static_cast<uint64_t>(C) * 2, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_mxfp8_quantize(
-      src_bf16, M, C, expert_off, E, q_e4m3, scales_e8m0, static_cast<long long>(Mcap),
+      tm_src, M, C, expert_off, E, q_e4m3, scales_e8m0, static_cast<long long>(Mcap),
       status_dev, dev.sms, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }

@@ -11,9 +11,10 @@ namespace mgw {
 constexpr int kMaxExperts = 1024;
 
 size_t quantize_smem_bytes(int E);
-cudaError_t launch_mxfp8_quantize(const void* src, int M, int C, const int32_t* expert_off, int E,
-                                  void* q, void* sc, long long Mcap, int* status, int num_sms,
-                                  cudaStream_t stream);
+// tm_src: bf16 [M, C] source, box 128 features x 128 tokens, no swizzle.
+cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, int M, int C,
+                                  const int32_t* expert_off, int E, void* q, void* sc,
+                                  long long Mcap, int* status, int num_sms, cudaStream_t stream);
 
 struct WgradArgs {
   CUtensorMap tm_a;    // g^T e4m3 [N, Mcap], box 128 tokens x 128 rows, 128B swizzle

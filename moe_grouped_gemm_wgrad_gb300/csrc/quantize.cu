@@ -2,11 +2,13 @@
 // [C, Mcap] (token-contiguous, per-expert 128-padded) + e8m0 scale atoms.
 //
 // HBM-bound transpose-quantize.  One work unit is 128 padded tokens x 128
-// features: it reads up to 32 KB of bf16 with 16-byte coalesced loads, finds
-// each (feature, 32-token block) maximum, scales by an exact power of two,
-// converts with the hardware's round-to-nearest-even saturating e4m3 convert,
-// and writes a 16 KB e4m3 tile (full 128-byte rows) plus one 512-byte scale
-// atom.  A persistent grid walks the units.
+// features.  A persistent grid walks the units; each CTA keeps two units' bf16
+// tiles (32 KB each) in flight with TMA loads, so HBM reads overlap the
+// conversion of the previous unit.  Per unit every thread owns one pair of
+// adjacent features and one 32-token block: 32-bit shared-memory reads, the
+// block maximum from the bf16 bits, an exact power-of-two scale, the hardware's
+// round-to-nearest-even saturating e4m3 convert.  The e4m3 tile leaves through
+// shared memory as full 128-byte rows, the 512-byte scale atom in one piece.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -19,10 +21,15 @@ namespace mgw {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kIn = 128 * 128 * 2;   // bf16 input tile [token][feature]
-constexpr int kOutPitch = 144;       // bytes per feature row of the e4m3 tile (128 + 16 pad)
-constexpr int kOut = 128 * kOutPitch;
+constexpr int kInBytes = 128 * 128 * 2;  // bf16 tile [token][feature], 256-byte rows
+constexpr int kInStages = 2;
+constexpr int kOutPitch = 144;           // bytes per feature row of the e4m3 tile (128 + 16 pad)
+constexpr int kOutBytes = 128 * kOutPitch;
 constexpr int kSf = 512;
+constexpr int kOffOut = kInStages * kInBytes;
+constexpr int kOffSf = kOffOut + kOutBytes;
+constexpr int kOffBar = kOffSf + kSf;
+constexpr int kOffTable = kOffBar + 8 * kInStages + 16;
 
 __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
@@ -30,112 +37,180 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float 
   return lo | (hi << 16);
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+// floor(log2 amax) is the bf16 exponent field minus 127 for normal values; the
+// scale byte is that minus 8 plus the bias 127, clamped at 0 (which also covers
+// amax == 0 and every subnormal amax).  Returns the byte; *inv = 2^(127 - byte).
+__device__ __forceinline__ int scale_byte(uint32_t amax_bits, float* inv) {
+  const int ef = static_cast<int>(amax_bits >> 7);
+  const int byte = ef > 8 ? ef - 8 : 0;
+  *inv = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);
+  return byte;
+}
 
-__global__ void __launch_bounds__(kThreads) mxfp8_quantize_kernel(
-    const uint16_t* __restrict__ src, int M, int C, const int32_t* __restrict__ expert_off, int E,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ sc, long long Mcap, int* status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);
-  uint8_t* s_out = smem + kIn;
-  uint8_t* s_sf = smem + kIn + kOut;
-  int* s_off = reinterpret_cast<int*>(smem + kIn + kOut + kSf);
+struct Unit {
+  int valid;  // tokens of the chunk that belong to the expert (0: padding-only chunk)
+  int row0;   // first source token
+};
+
+__device__ __forceinline__ Unit locate(int ch, int used_chunks, const int* s_off, const int* s_pad,
+                                       int E) {
+  Unit u{0, 0};
+  if (ch < used_chunks) {
+    // the largest e with P[e] <= 128*ch: always a non-empty expert for a used chunk
+    const int t0 = ch * 128;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pad[mid] <= t0)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int tin = t0 - s_pad[lo];
+    u.valid = min(128, s_off[lo + 1] - s_off[lo] - tin);
+    u.row0 = s_off[lo] + tin;
+  }
+  return u;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
+    const __grid_constant__ CUtensorMap tm_src, int M, int C, const int32_t* __restrict__ expert_off,
+    int E, uint8_t* __restrict__ q, uint8_t* __restrict__ sc, long long Mcap, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  // TMA destinations want 128-byte alignment; the launch adds 128 bytes of slack.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const uint32_t sbase = smem_u32(smem);
+  uint8_t* s_out = smem + kOffOut;
+  uint8_t* s_sf = smem + kOffSf;
+  int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 8 * kInStages);  // [0] flag [1] abort
+  int* s_off = reinterpret_cast<int*>(smem + kOffTable);
   int* s_pad = s_off + (E + 1);
-  int* s_flag = s_pad + (E + 1);
-  if (!load_offsets(expert_off, E, M, s_off, s_pad, s_flag, status)) return;
-
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_misc[1]);
   const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_misc[1] = 0;
+    for (int s = 0; s < kInStages; ++s) mbar_init(sbase + kOffBar + 8 * s, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_src);
+  }
+  if (!load_offsets(expert_off, E, M, s_off, s_pad, &s_misc[0], status)) return;
+
   const int col_tiles = C / 128;
   const long long units = (Mcap / 128) * col_tiles;
   const int used_chunks = s_pad[E] / 128;
+  const long long stride = gridDim.x;
 
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+  // Issue the TMA load of unit u into input stage s (rows past the expert are read but
+  // masked; rows past M come back as zeros).  Padding-only units load nothing.
+  auto issue = [&](long long u, int s) {
     const int ch = static_cast<int>(u / col_tiles);
     const int ct = static_cast<int>(u % col_tiles);
-    // Expert of this 128-token chunk of the padded axis: the largest e with
-    // P[e] <= 128*ch (always a non-empty expert when the chunk is in use).
-    int valid = 0, row0 = 0;
-    if (ch < used_chunks) {
-      const int t0 = ch * 128;
-      int lo = 0, hi = E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_pad[mid] <= t0)
-          lo = mid;
-        else
-          hi = mid - 1;
-      }
-      const int tin = t0 - s_pad[lo];
-      const int cnt = s_off[lo + 1] - s_off[lo];
-      valid = min(128, cnt - tin);
-      row0 = s_off[lo] + tin;
+    const Unit un = locate(ch, used_chunks, s_off, s_pad, E);
+    const uint32_t bar = sbase + kOffBar + 8 * s;
+    if (un.valid > 0) {
+      mbar_arrive_expect_tx(bar, kInBytes);
+      tma_load_2d(sbase + s * kInBytes, &tm_src, ct * 128, un.row0, bar);
+    } else {
+      mbar_arrive(bar);
     }
-    // Load the bf16 tile: 128 tokens x 16 x 16 B; tokens past the expert's end are zero.
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kInStages; ++s) {
+      const long long u = blockIdx.x + s * stride;
+      if (u < units) issue(u, s);
+    }
+  }
+
+  const int p = tid & 63;   // feature pair: features 2p, 2p+1 of the tile
+  const int kb = tid >> 6;  // 32-token block of the chunk
+  uint32_t phase = 0;
+  int stage = 0;
+  for (long long u = blockIdx.x; u < units; u += stride) {
+    const int ch = static_cast<int>(u / col_tiles);
+    const int ct = static_cast<int>(u % col_tiles);
+    const Unit un = locate(ch, used_chunks, s_off, s_pad, E);
+    // Every thread waits; the decision to give up is made uniformly for the block.
+    const int timed_out = mbar_wait(sbase + kOffBar + 8 * stage, phase, abort_flag) ? 0 : 1;
+    if (__syncthreads_or(timed_out)) {
+      // Only reachable if a TMA load never lands; report and stop this CTA's work.
+      if (tid == 0) {
+        if (status) atomicOr(status, kDevTimeout);
+        *abort_flag = 1;
+      }
+      break;
+    }
+    const uint32_t* in = reinterpret_cast<const uint32_t*>(smem + stage * kInBytes);
+    uint32_t v[32];
+    uint32_t amax_lo = 0, amax_hi = 0;
+    const int nvalid = min(32, max(0, un.valid - kb * 32));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + i * kThreads;
-      const int r = idx >> 4, c16 = idx & 15;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < valid)
-        v = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row0 + r) * C +
-                                                 ct * 128 + c16 * 8));
-      *reinterpret_cast<uint4*>(s_in + r * 128 + c16 * 8) = v;
+    for (int i = 0; i < 32; ++i) {
+      v[i] = (i < nvalid) ? in[(kb * 32 + i) * 64 + p] : 0u;  // bf16 pair (2p low, 2p+1 high)
+      amax_lo = max(amax_lo, v[i] & 0x7FFFu);                // |bf16| orders like its bits
+      amax_hi = max(amax_hi, (v[i] >> 16) & 0x7FFFu);
+    }
+    float inv_lo, inv_hi;
+    const int byte_lo = scale_byte(amax_lo, &inv_lo);
+    const int byte_hi = scale_byte(amax_hi, &inv_hi);
+    uint32_t pl[8], ph[8];
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      pl[i / 4] = cvt_e4m3x4(__uint_as_float(v[i] << 16) * inv_lo, __uint_as_float(v[i + 1] << 16) * inv_lo,
+                             __uint_as_float(v[i + 2] << 16) * inv_lo, __uint_as_float(v[i + 3] << 16) * inv_lo);
+      ph[i / 4] = cvt_e4m3x4(__uint_as_float(v[i] & 0xFFFF0000u) * inv_hi,
+                             __uint_as_float(v[i + 1] & 0xFFFF0000u) * inv_hi,
+                             __uint_as_float(v[i + 2] & 0xFFFF0000u) * inv_hi,
+                             __uint_as_float(v[i + 3] & 0xFFFF0000u) * inv_hi);
+    }
+    __syncthreads();  // every thread has read input stage `stage`; the output tile is free
+    if (tid == 0) {
+      const long long nu = u + kInStages * stride;
+      if (nu < units) issue(nu, stage);
+    }
+    {
+      uint4* r0 = reinterpret_cast<uint4*>(s_out + (2 * p) * kOutPitch + kb * 32);
+      uint4* r1 = reinterpret_cast<uint4*>(s_out + (2 * p + 1) * kOutPitch + kb * 32);
+      r0[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+      r0[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+      r1[0] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+      r1[1] = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+      const int c0 = 2 * p, c1 = 2 * p + 1;
+      s_sf[(c0 & 31) * 16 + (c0 >> 5) * 4 + kb] = static_cast<uint8_t>(byte_lo);
+      s_sf[(c1 & 31) * 16 + (c1 >> 5) * 4 + kb] = static_cast<uint8_t>(byte_hi);
     }
     __syncthreads();
-    // Quantize: thread -> feature c, two 32-token blocks.
-    const int c = tid & 127;
-#pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-      const int kb = (tid >> 7) * 2 + bb;
-      uint32_t h[32];
-      uint32_t amax = 0;
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        h[t] = s_in[(kb * 32 + t) * 128 + c];
-        amax = max(amax, h[t] & 0x7FFFu);  // |bf16| orders like its bits (finite values)
-      }
-      // floor(log2 amax) = exponent field - 127 for normal bf16; the scale byte is
-      // that minus 8 plus the bias 127, clamped at 0 (which also covers amax == 0
-      // and every subnormal amax).
-      const int ef = static_cast<int>(amax >> 7);
-      const int byte = ef > 8 ? ef - 8 : 0;
-      const float inv = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^(127-byte)
-      uint32_t pk[8];
-#pragma unroll
-      for (int t = 0; t < 32; t += 4)
-        pk[t / 4] = cvt_e4m3x4(bf16_bits_to_float(h[t]) * inv, bf16_bits_to_float(h[t + 1]) * inv,
-                               bf16_bits_to_float(h[t + 2]) * inv, bf16_bits_to_float(h[t + 3]) * inv);
-      uint4* dst = reinterpret_cast<uint4*>(s_out + c * kOutPitch + kb * 32);
-      dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      s_sf[(c & 31) * 16 + ((c >> 5) & 3) * 4 + kb] = static_cast<uint8_t>(byte);
-    }
-    __syncthreads();
-    // Store: 128 feature rows x 128 B (8 threads per row), then the 512-byte atom.
+    // 128 feature rows x 128 B (8 threads per row), then the 512-byte atom.
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = (tid >> 3) + i * 32, c16 = tid & 7;
-      const uint4 v = *reinterpret_cast<const uint4*>(s_out + r * kOutPitch + c16 * 16);
+      const uint4 w = *reinterpret_cast<const uint4*>(s_out + r * kOutPitch + c16 * 16);
       *reinterpret_cast<uint4*>(q + static_cast<size_t>(ct * 128 + r) * static_cast<size_t>(Mcap) +
-                                static_cast<size_t>(ch) * 128 + c16 * 16) = v;
+                                static_cast<size_t>(ch) * 128 + c16 * 16) = w;
     }
     if (tid < 32) {
-      const uint4 v = *reinterpret_cast<const uint4*>(s_sf + tid * 16);
-      *reinterpret_cast<uint4*>(sc + (static_cast<size_t>(ch) * col_tiles + ct) * kSf + tid * 16) = v;
+      const uint4 w = *reinterpret_cast<const uint4*>(s_sf + tid * 16);
+      *reinterpret_cast<uint4*>(sc + (static_cast<size_t>(ch) * col_tiles + ct) * kSf + tid * 16) = w;
     }
-    __syncthreads();
+    if (++stage == kInStages) stage = 0, phase ^= 1u;
+  }
+  // Loads issued for units this CTA never reached (only after an abort) must land
+  // before the CTA exits.
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    int never = 0;
+    for (int s = 0; s < kInStages; ++s) (void)mbar_wait(sbase + kOffBar + 8 * s, phase, &never);
   }
 }
 
 }  // namespace
 
 size_t quantize_smem_bytes(int E) {
-  return static_cast<size_t>(kIn + kOut + kSf) + sizeof(int) * (2 * (E + 1) + 1);
+  return static_cast<size_t>(kOffTable) + sizeof(int) * (2 * (E + 1)) + 128;
 }
 
-cudaError_t launch_mxfp8_quantize(const void* src, int M, int C, const int32_t* expert_off, int E,
-                                  void* q, void* sc, long long Mcap, int* status, int num_sms,
-                                  cudaStream_t stream) {
+cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, int M, int C,
+                                  const int32_t* expert_off, int E, void* q, void* sc,
+                                  long long Mcap, int* status, int num_sms, cudaStream_t stream) {
   const size_t smem = quantize_smem_bytes(E);
   static thread_local int attr_set_device = -1;
   int dev = 0;
@@ -156,8 +231,7 @@ cudaError_t launch_mxfp8_quantize(const void* src, int M, int C, const int32_t* 
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
   mxfp8_quantize_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
-      static_cast<const uint16_t*>(src), M, C, expert_off, E, static_cast<uint8_t*>(q),
-      static_cast<uint8_t*>(sc), Mcap, status);
+      tm_src, M, C, expert_off, E, static_cast<uint8_t*>(q), static_cast<uint8_t*>(sc), Mcap, status);
   return cudaGetLastError();
 }
 
