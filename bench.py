@@ -353,7 +353,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     peaks = _peaks()
-    mxfp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+    # nominal fp8 : bf16 dense ratio 4.5 : 2.25; the sustained figure applies to a kernel
+    # timed inside a long loop (the default timed region runs about a second under load)
+    mxfp8_burst = 2.0 * peaks["bf16_tflops"]
+    mxfp8_sustained = 2.0 * (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"])
     metric = "MXFP8 grouped wgrad TFLOP/s"
     d = Dist()
 
@@ -399,6 +402,10 @@ def main():
     case = r["case"]
     value = r["flops"] * d.world / (r["ms_per_step"] * 1e-3) / 1e12
     wg_tflops = r["flops"] / (r["wgrad_ms"] * 1e-3) / 1e12
+    long_region = r["ms_per_step"] * args.steps >= 500.0
+    power_capped = bool(r["clocks"]) and "sw_power_cap" in r["clocks"].get("reasons", [])
+    peak_kind = "sustained" if (long_region or power_capped) else "burst"
+    mxfp8_peak = mxfp8_sustained if peak_kind == "sustained" else mxfp8_burst
     cpu = None
     if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
@@ -415,8 +422,11 @@ def main():
             "roofline": {"bound": "tensor", "achieved": wg_tflops, "peak": mxfp8_peak,
                          "unit": "TFLOP/s", "frac": wg_tflops / mxfp8_peak,
                          "traffic": _traffic("grouped_wgrad_kernel", ["wgrad.cu", "ptx.cuh", "common.cuh"]),
-                         "kernel": "grouped_wgrad_kernel",
-                         "peak_note": f"2 x bf16 dense {peaks['bf16_tflops']} TFLOP/s ({peaks['source']}, burst)"},
+                         "kernel": "grouped_wgrad_kernel", "peak_kind": peak_kind,
+                         "frac_of_burst": wg_tflops / mxfp8_burst,
+                         "algorithmic_bytes": r["wgrad_min_bytes"],
+                         "peak_note": f"2 x measured bf16 dense ({peaks['source']}): burst {mxfp8_burst:.1f}, "
+                                      f"sustained {mxfp8_sustained:.1f} TFLOP/s; fp8:bf16 nominal ratio 2"},
             "kernels_ms": {"mxfp8_quantize_g": r["quant_g_ms"], "mxfp8_quantize_x": r["quant_x_ms"],
                            "grouped_wgrad": r["wgrad_ms"], "grouped_wgrad_median": r["wgrad_ms_median"]},
             "quantize_hbm": {"achieved_gbs": r["quant_bytes"] / ((r["quant_g_ms"] + r["quant_x_ms"]) * 1e-3) / 1e9,

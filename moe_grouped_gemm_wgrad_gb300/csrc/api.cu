@@ -150,8 +150,14 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* x
   std::memset(&a, 0, sizeof(a));
   if (!make_map_2d(&a.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, Mcap, N, Mcap, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128, 256,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128,
+                   mgw::wgrad_uses_pair(N) ? 128 : 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a.tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, 256,
+                   static_cast<uint64_t>(N) * (Mcap / 32) / 256, 256, 256, 2,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&a.tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, 256,
+                   static_cast<uint64_t>(K) * (Mcap / 32) / 256, 256, 256, 4,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(&a.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_bf16, K,
                    static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       constexpr uint32_t idesc = idesc_tf32(BM, BN);
       for (long long it = blockIdx.x; it < total && ok; it += gridDim.x, ++local) {
         const int b = local & 1;
-        if (!mbar_wait(bar_acc_empty(b), acc_phase[b] ^ 1u, abort_flag)) {
+        if (!mbar_wait_spin(bar_acc_empty(b), acc_phase[b] ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
         tc_fence_after();
         const uint32_t dacc = tmem + 256u * b;
         for (int c = 0; c < nchunks; ++c) {
-          if (!mbar_wait(bar_full(stage), phase, abort_flag)) {
+          if (!mbar_wait_spin(bar_full(stage), phase, abort_flag)) {
             ok = false;
             break;
           }

@@ -16,9 +16,15 @@ cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, int M, int C,
                                   const int32_t* expert_off, int E, void* q, void* sc,
                                   long long Mcap, int* status, int num_sms, cudaStream_t stream);
 
+// True when grad_w tiles go to CTA pairs (tcgen05 cta_group::2); this sets the box
+// height of tm_b (128 rows for pairs, 256 otherwise) and whether tm_sfa/tm_sfb are used.
+bool wgrad_uses_pair(int N);
+
 struct WgradArgs {
   CUtensorMap tm_a;    // g^T e4m3 [N, Mcap], box 128 tokens x 128 rows, 128B swizzle
-  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x 256 rows, 128B swizzle
+  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x (128 or 256) rows, 128B swizzle
+  CUtensorMap tm_sfa;  // g scale atoms as 256-byte rows, box 256 x 2 (one atom)
+  CUtensorMap tm_sfb;  // x scale atoms as 256-byte rows, box 256 x 4 (two atoms)
   CUtensorMap tm_out;  // grad_w bf16 [E*N, K], box 64 cols x 128 rows, 128B swizzle
   const uint8_t* gs;   // g scale atoms
   const uint8_t* xs;   // x scale atoms

@@ -127,3 +127,10 @@ def test_wgrad_bad_offsets_reported_and_output_untouched():
     torch.cuda.synchronize()
     assert int(status.item()) & mgw.MGW_DEV_BAD_OFFSETS
     assert bool((out == 3.0).all())
+
+
+def test_wgrad_cta_pair_kernel_matches_oracle(monkeypatch):
+    """The opt-in CTA-pair kernel (tcgen05 cta_group::2) on shapes with N % 256 == 0."""
+    monkeypatch.setenv("MGW_WGRAD_CTA_PAIRS", "1")
+    _check_full(synth.wgrad_random(463, 256, 512, [0, 1, 129, 300, 33], seed=41))
+    _check_full(synth.wgrad_random(384, 512, 256, [256, 0, 128], seed=42, outlier_frac=0.01))
