@@ -21,9 +21,10 @@
 //               tcgen05.mma.kind::tf32 (M=128, N=256, K=8) into one of two TMEM
 //               accumulators (2 x 256 columns), so the epilogue of one item
 //               overlaps the main loop of the next.
-//   warps 5-12  transform: load dy and W tiles from global memory, split into
-//               hi/lo, write K-major 128B-swizzled tiles (W transposed on the
-//               fly) into a 2-stage shared-memory ring.
+//   warps 5-12  transform: load dy and W tiles from global memory one chunk ahead
+//               (software pipelined in registers), split into hi/lo, write K-major
+//               128B-swizzled tiles (W transposed on the fly) into a 2-stage
+//               shared-memory ring.
 #include <cstdint>
 
 #include "common.cuh"
@@ -155,71 +156,96 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
 
   if (warp >= kEpiWarps + 1) {
     // ----------------------------------------------------------- transform
+    // Software-pipelined: the global loads of the next chunk (possibly of the next item)
+    // are in flight while the current chunk is split and written to shared memory.
     const int xt = tid - (kEpiWarps + 1) * 32;  // 0..255
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const Item item = decode_item(it, tiles_k, s_rtp, E);
+    // raw operands of one chunk in registers: dy 4 x float4, W 8 x 4 floats
+    struct Raw {
+      float4 a[4];
+      float b[8][4];
+    };
+    auto load_chunk = [&](const Item& item, int c, Raw& raw) {
       const int row0 = s_off[item.e] + item.rt * BM;
       const int valid = min(BM, s_off[item.e + 1] - row0);
-      const float* Wk = args.W + static_cast<size_t>(item.e) * out_f * in_f + item.kt * BN;
-      for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t s_ahi = sbase + stage * kStageBytes;
-        const uint32_t s_alo = s_ahi + kATile;
-        const uint32_t s_bhi = s_alo + kATile;
-        const uint32_t s_blo = s_bhi + kBTile;
-        // A = dy[row0 .. row0+127, 32c .. 32c+31]: 128 rows x 8 chunks of 16 B.
-        float4 av[4];
+      // A = dy[row0 .. row0+127, 32c .. 32c+31]: 128 rows x 8 chunks of 16 B.
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int idx = xt + p * 256;
-          const int r = idx >> 3, j = idx & 7;
-          av[p] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (r < valid)
-            av[p] = __ldg(reinterpret_cast<const float4*>(
-                args.dy + static_cast<size_t>(row0 + r) * out_f + c * BK + 4 * j));
-        }
-        // B^T tile: for dx column k (= K-major row k of B) and 4 consecutive n.
-        // Lane -> k (32 consecutive k per warp), 8 (k-block, n-group) pairs per thread.
-        float bv[8][4];
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int idx = xt + p * 256;      // 0..2047
-          const int k = idx & 255, ng = idx >> 8;  // ng in 0..7
-          const float* src = Wk + static_cast<size_t>(c * BK + 4 * ng) * in_f + k;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) bv[p][q] = __ldg(src + static_cast<size_t>(q) * in_f);
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int idx = xt + p * 256;
-          const int r = idx >> 3, j = idx & 7;
-          uint4 hi, lo;
-          split4(av[p], hi, lo);
-          const uint32_t off = r * 128 + ((j ^ (r & 7)) << 4);
-          st_shared_u4(s_ahi + off, hi);
-          st_shared_u4(s_alo + off, lo);
-        }
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int idx = xt + p * 256;
-          const int k = idx & 255, ng = idx >> 8;
-          uint4 hi, lo;
-          split4(make_float4(bv[p][0], bv[p][1], bv[p][2], bv[p][3]), hi, lo);
-          const uint32_t off = k * 128 + ((ng ^ (k & 7)) << 4);
-          st_shared_u4(s_bhi + off, hi);
-          st_shared_u4(s_blo + off, lo);
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_full(stage));
-        if (++stage == kStages) stage = 0, phase ^= 1u;
+      for (int p = 0; p < 4; ++p) {
+        const int idx = xt + p * 256;
+        const int r = idx >> 3, j = idx & 7;
+        raw.a[p] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < valid)
+          raw.a[p] = __ldg(reinterpret_cast<const float4*>(
+              args.dy + static_cast<size_t>(row0 + r) * out_f + c * BK + 4 * j));
       }
+      // B^T tile: dx column k (K-major row k of B) and 4 consecutive n; lane -> k.
+      const float* Wk = args.W + static_cast<size_t>(item.e) * out_f * in_f + item.kt * BN;
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const int idx = xt + p * 256;            // 0..2047
+        const int k = idx & 255, ng = idx >> 8;  // ng in 0..7
+        const float* src = Wk + static_cast<size_t>(c * BK + 4 * ng) * in_f + k;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) raw.b[p][q] = __ldg(src + static_cast<size_t>(q) * in_f);
+      }
+    };
+    long long it = blockIdx.x;
+    Raw cur, nxt;
+    Item item{0, 0, 0};
+    int c = 0;
+    if (it < total) {
+      item = decode_item(it, tiles_k, s_rtp, E);
+      load_chunk(item, 0, cur);
+    }
+    while (it < total && ok) {
+      // the chunk after (item, c): next chunk of this item, else chunk 0 of the next item
+      long long nit = it;
+      int nc = c + 1;
+      Item nitem = item;
+      if (nc == nchunks) {
+        nc = 0;
+        nit = it + gridDim.x;
+        if (nit < total) nitem = decode_item(nit, tiles_k, s_rtp, E);
+      }
+      if (nit < total) load_chunk(nitem, nc, nxt);
+      if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t s_ahi = sbase + stage * kStageBytes;
+      const uint32_t s_alo = s_ahi + kATile;
+      const uint32_t s_bhi = s_alo + kATile;
+      const uint32_t s_blo = s_bhi + kBTile;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int idx = xt + p * 256;
+        const int r = idx >> 3, j = idx & 7;
+        uint4 hi, lo;
+        split4(cur.a[p], hi, lo);
+        const uint32_t off = r * 128 + ((j ^ (r & 7)) << 4);
+        st_shared_u4(s_ahi + off, hi);
+        st_shared_u4(s_alo + off, lo);
+      }
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const int idx = xt + p * 256;
+        const int k = idx & 255, ng = idx >> 8;
+        uint4 hi, lo;
+        split4(make_float4(cur.b[p][0], cur.b[p][1], cur.b[p][2], cur.b[p][3]), hi, lo);
+        const uint32_t off = k * 128 + ((ng ^ (k & 7)) << 4);
+        st_shared_u4(s_bhi + off, hi);
+        st_shared_u4(s_blo + off, lo);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_full(stage));
+      if (++stage == kStages) stage = 0, phase ^= 1u;
+      it = nit;
+      c = nc;
+      item = nitem;
+      cur = nxt;
     }
     if (!ok) {
       *abort_flag = 1;
