@@ -46,49 +46,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// One try_wait with a suspend-time hint: the thread sleeps until the phase completes or
+// about kSuspendNs pass.  Measured on GB300: a try_wait WITHOUT a hint in the thread that
+// issues tcgen05.mma halves the MMA rate even when the phase has already completed; with
+// the hint it costs nothing.
+constexpr uint32_t kSuspendNs = 1000000;  // 1 ms per try
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Gives up (returns
-// false) after kWaitLimitNs, or at once when *abort is set by another role.
+// Waits for the phase with the given parity to complete.  Gives up (returns false) after
+// kWaitLimitNs, or soon after *abort is set by another role.  The clock and the abort flag
+// are read only every 4 tries, i.e. after real waiting.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// Non-blocking probe of a phase (acquire semantics, like try_wait).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Same contract as mbar_wait, for the thread that issues tcgen05.mma.  It spins on
-// test_wait alone and looks at the abort flag and the clock only every 1024 polls:
-// measured on GB300, a blocking try_wait, a nanosleep or a %globaltimer read inside
-// this thread's wait loop slows the MMAs it has already queued (to about half rate
-// while it waits), a bare test_wait loop does not.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort) {
-  uint32_t polls = 0;
+  uint32_t tries = 0;
   uint64_t t0 = 0;
-  while (!mbar_test_wait(bar, parity)) {
-    if ((++polls & 1023u) == 0) {
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++tries & 3u) == 0) {
       if (*abort) return false;
       const uint64_t now = globaltimer();
       if (t0 == 0) t0 = now;
@@ -96,6 +77,10 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, vo
     }
   }
   return true;
+}
+// The MMA-issuing threads use the same hinted wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait(bar, parity, abort);
 }
 
 // ----------------------------------------------------------------------- TMA
