@@ -162,6 +162,7 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* x
                    static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return MGW_ERR_CUDA;
+  a.out = out_bf16;
   a.gs = static_cast<const uint8_t*>(gs);
   a.xs = static_cast<const uint8_t*>(xs);
   a.expert_off = expert_off;

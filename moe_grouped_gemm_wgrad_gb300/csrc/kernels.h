@@ -26,6 +26,7 @@ struct WgradArgs {
   CUtensorMap tm_sfa;  // g scale atoms as 256-byte rows, box 256 x 2 (one atom)
   CUtensorMap tm_sfb;  // x scale atoms as 256-byte rows, box 256 x 4 (two atoms)
   CUtensorMap tm_out;  // grad_w bf16 [E*N, K], box 64 cols x 128 rows, 128B swizzle
+  void* out;           // grad_w (plain stores of the zero tiles)
   const uint8_t* gs;   // g scale atoms
   const uint8_t* xs;   // x scale atoms
   const int32_t* expert_off;

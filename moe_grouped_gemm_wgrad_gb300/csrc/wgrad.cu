@@ -4,11 +4,11 @@
 //
 // Work item = (expert, 128-row N tile, 256-column K tile); one item's output tile
 // is a 128 x 256 fp32 accumulator in TMEM (256 columns).  A persistent grid of one
-// CTA per SM walks the items in a static stride, experts ordered by descending
-// token count so the largest experts are spread first (LPT); experts with no
-// tokens become store-only items that write zero rows.
+// CTA per SM walks the items in a snake order over the experts sorted by descending
+// token count (LPT), so the largest experts are spread first; experts with no tokens
+// become store-only items that write zero rows.
 //
-// Roles (320 threads):
+// Roles (352 threads):
 //   warp 0      TMA producer: per 128-token chunk, g^T tile 128x128 B, x^T tile
 //               256x128 B (both 128B-swizzled) and the two e8m0 scale-factor atom
 //               sets (512 B + 1 KB) into a 4-stage shared-memory ring.
@@ -16,6 +16,8 @@
 //               32x128b.warpx4) and issues one block-scaled
 //               tcgen05.mma.kind::mxf8f6f4 (M=128, N=256, K=32) per 32-token block
 //               that holds tokens, then commits the stage back to the producer.
+//   warp 10     zero writer: stores the rows of experts without tokens with plain
+//               vector stores, overlapping the MMA work (single-SM kernel).
 //   warps 2-9   epilogue: drain the accumulator (each warp: its TMEM lane quarter,
 //               one 128-column half) into registers, release TMEM at once so the
 //               next item's MMAs start, then round to bf16 and TMA-store the tile as
@@ -47,8 +49,9 @@ constexpr int kOffBar = kOffSf + kStages * kSfStage;
 constexpr int kNumBars = 2 * kStages + 3;        // full[], empty[], acc_full, acc_empty, done
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffTable = kOffMisc + 16;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kEpiWarps = 8;
+constexpr int kZeroWarp = 10;  // single-SM kernel: writes the tiles of experts without tokens
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;  // scale slots: 16 TMEM columns per stage
 
@@ -71,6 +74,26 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                "r"(d)
                : "memory");
 }
+
+// Snake order over the LPT-sorted items: round r hands items to CTAs left to right when r is
+// even and right to left when r is odd, so the heaviest items do not all land on the same
+// CTAs.  Every role of a CTA walks the same sequence.
+struct ItemIter {
+  long long total, grid, round;
+  int cta;
+  __device__ __forceinline__ bool next(long long& it) {
+    while (true) {
+      const long long base = round * grid;
+      if (base >= total) return false;
+      const long long idx = base + ((round & 1) ? (grid - 1 - cta) : cta);
+      ++round;
+      if (idx < total) {
+        it = idx;
+        return true;
+      }
+    }
+  }
+};
 
 // Waits without honouring the abort flag (used to drain in-flight async work).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -146,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       uint32_t pending_phase[kStages];
       for (int s = 0; s < kStages; ++s) pending[s] = 0, pending_phase[s] = 0;
       bool ok = true;
-      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
+      long long it = 0;
+      while (ok && items.next(it)) {
         const int e = s_order[it / per_expert];
         const int tile = static_cast<int>(it % per_expert);
         const int nt = tile / tiles_k, kt = tile % tiles_k;
@@ -201,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
         tmem_cp_32x128b_warpx4(tsf + 12, make_sdesc(ssf + 1024, 0, 128, 0));
         return true;
       };
-      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
+      long long it = 0;
+      while (ok && items.next(it)) {
         const int e = s_order[it / per_expert];
         const int cnt = s_off[e + 1] - s_off[e];
         if (cnt == 0) continue;
@@ -242,6 +269,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       mma_commit(bar_done);
       mbar_wait_drain(bar_done, 0);
     }
+  } else if (warp == kZeroWarp) {
+    // ----------------------------------------- zero tiles of experts without tokens
+    // Plain 16-byte stores (one 512-byte row segment per instruction) that overlap the
+    // MMA work of the other roles instead of queueing behind it in the epilogue.
+    uint8_t* out = static_cast<uint8_t*>(args.out);
+    const size_t pitch = static_cast<size_t>(K) * 2;
+    ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
+    long long it = 0;
+    while (items.next(it)) {
+      const int e = s_order[it / per_expert];
+      if (s_off[e + 1] != s_off[e]) continue;
+      const int tile = static_cast<int>(it % per_expert);
+      const int nt = tile / tiles_k, kt = tile % tiles_k;
+      uint8_t* base = out + (static_cast<size_t>(e) * N + nt * BM) * pitch +
+                      static_cast<size_t>(kt) * BN * 2 + lane * 16;
+#pragma unroll 4
+      for (int r = 0; r < BM; ++r)
+        *reinterpret_cast<uint4*>(base + r * pitch) = make_uint4(0u, 0u, 0u, 0u);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
@@ -250,11 +296,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
     const int row = quarter * 32 + static_cast<int>(lane);
     const bool leader = (ew == 0 && lane == 0);
     uint32_t acc_phase = 0;
-    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+    ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
+    long long it = 0;
+    while (items.next(it)) {
       const int e = s_order[it / per_expert];
       const int tile = static_cast<int>(it % per_expert);
       const int nt = tile / tiles_k, kt = tile % tiles_k;
       const int cnt = s_off[e + 1] - s_off[e];
+      if (cnt == 0) continue;  // written by the zero warp
       uint32_t pk[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) pk[j] = 0u;
@@ -342,7 +391,9 @@ __host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
 }
 static_assert(wgrad_pair_smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
 
-__global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_pair_kernel(const __grid_constant__ WgradArgs args) {
+constexpr int kPThreads = 320;
+
+__global__ void __launch_bounds__(kPThreads, 1) grouped_wgrad_pair_kernel(const __grid_constant__ WgradArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -362,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_pair_kernel(const _
   // Both CTAs see the same offsets, so both take the same branch here.
   if (!load_offsets(args.expert_off, E, args.M, s_off, s_pad, &s_misc[2], args.status)) return;
 
-  for (int e = tid; e < E; e += kThreads) {
+  for (int e = tid; e < E; e += kPThreads) {
     const int ce = s_off[e + 1] - s_off[e];
     int rank_e = 0;
     for (int j = 0; j < E; ++j) {
@@ -622,7 +673,7 @@ cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t s
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kPThreads, 1, 1);
   cfg.dynamicSmemBytes = wgrad_pair_smem_bytes(a.E);
   cfg.stream = stream;
   cfg.attrs = attr;
