@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -171,6 +172,10 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* x
   a.N = N;
   a.K = K;
   a.status = status_dev;
+  {
+    const char* v = std::getenv("MGW_TEST_DROP_LOAD");  // test hook, see kernels.h
+    a.drop_first_load = (v != nullptr && v[0] == '1') ? 1 : 0;
+  }
   const cudaError_t err = mgw::launch_grouped_wgrad(a, dev.sms, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }

@@ -32,6 +32,10 @@ struct WgradArgs {
   const int32_t* expert_off;
   int E, M, N, K;
   int* status;
+  // Test hook for the device time limit: when set, the single-SM kernel's producer
+  // announces its first chunk's bytes but never issues the copies, so the waits on that
+  // stage run out and the kernel reports MGW_DEV_TIMEOUT.  Zero in normal use.
+  int drop_first_load;
 };
 cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream);
 

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       int pending[kStages];
       uint32_t pending_phase[kStages];
       for (int s = 0; s < kStages; ++s) pending[s] = 0, pending_phase[s] = 0;
-      bool ok = true;
+      bool ok = true, dropped = false;
       ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
       long long it = 0;
       while (ok && items.next(it)) {
@@ -186,6 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
           }
           const uint32_t fb = bar_full(stage);
           mbar_arrive_expect_tx(fb, kStageBytes + kSfStage);
+          if (args.drop_first_load && !dropped) {  // test hook: this stage never fills
+            dropped = true;
+            pending[stage] = 1;
+            pending_phase[stage] = phase;
+            if (++stage == kStages) stage = 0, phase ^= 1u;
+            continue;
+          }
           const uint32_t sa = sbase + stage * kStageBytes;
           const int tok = (ch0 + c) * BT;
           tma_load_2d(sa, &args.tm_a, tok, nt * BM, fb);

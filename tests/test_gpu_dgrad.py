@@ -82,3 +82,12 @@ def test_dgrad_bad_offsets_reported_and_output_untouched():
     torch.cuda.synchronize()
     assert int(status.item()) & mgw.MGW_DEV_BAD_OFFSETS
     assert bool((dx == 7.0).all())
+
+
+def test_dgrad_max_experts():
+    rng = np.random.default_rng(46)
+    counts = np.where(rng.random(1024) < 0.2, rng.integers(1, 30, 1024), 0)
+    case = synth.dgrad_random(int(counts.sum()), 32, 256, counts, seed=46)
+    dx = _gpu_dgrad(case).cpu().numpy().astype(np.float64)
+    ref, bound = oracle.grouped_dgrad(case.dy, case.W, case.expert_off)
+    assert np.all(np.abs(dx - ref) <= 1e-5 * bound)

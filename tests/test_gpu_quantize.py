@@ -97,3 +97,10 @@ def test_quantize_bad_offsets_reported_and_output_untouched():
         torch.cuda.synchronize()
         assert int(status.item()) & mgw.MGW_DEV_BAD_OFFSETS
         assert bool((q == 0xAB).all()) and bool((sc == 0xCD).all())
+
+
+def test_quantize_max_experts():
+    rng = np.random.default_rng(45)
+    counts = np.where(rng.random(1024) < 0.2, rng.integers(1, 70, 1024), 0)
+    case = synth.wgrad_random(int(counts.sum()), 256, 128, counts, seed=45)
+    _check(case.g_bf16, case.expert_off)

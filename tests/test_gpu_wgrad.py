@@ -134,3 +134,29 @@ def test_wgrad_cta_pair_kernel_matches_oracle(monkeypatch):
     monkeypatch.setenv("MGW_WGRAD_CTA_PAIRS", "1")
     _check_full(synth.wgrad_random(463, 256, 512, [0, 1, 129, 300, 33], seed=41))
     _check_full(synth.wgrad_random(384, 512, 256, [256, 0, 128], seed=42, outlier_frac=0.01))
+
+
+def test_wgrad_max_experts():
+    """E = 1024 (the library's maximum), mostly empty experts, ragged counts."""
+    rng = np.random.default_rng(43)
+    counts = np.where(rng.random(1024) < 0.15, rng.integers(1, 40, 1024), 0)
+    _check_full(synth.wgrad_random(int(counts.sum()), 128, 256, counts, seed=43))
+
+
+def test_wgrad_device_time_limit_reports_and_context_survives(monkeypatch):
+    """A pipeline stage that never fills makes the kernel's bounded waits run out: the
+    call reports MGW_DEV_TIMEOUT in the status word instead of hanging, and the CUDA
+    context stays usable for the next call."""
+    case = synth.wgrad_random(256, 128, 256, [128, 128], seed=44)
+    off = dev_i32(case.expert_off)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gq, gs = mgw.mxfp8_quantize(dev_bf16(case.g_bf16), off, status=status)
+    xq, xs = mgw.mxfp8_quantize(dev_bf16(case.x_bf16), off, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    monkeypatch.setenv("MGW_TEST_DROP_LOAD", "1")
+    mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, case.M, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & mgw.MGW_DEV_TIMEOUT
+    monkeypatch.delenv("MGW_TEST_DROP_LOAD")
+    _check_full(case)
