@@ -126,9 +126,13 @@ mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t*
                    M > 0 ? static_cast<uint64_t>(M) : 1, static_cast<uint64_t>(C) * 2, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return MGW_ERR_CUDA;
+  CUtensorMap tm_q;
+  if (!make_map_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_e4m3, Mcap, C, Mcap, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_mxfp8_quantize(
-      tm_src, M, C, expert_off, E, q_e4m3, scales_e8m0, static_cast<long long>(Mcap),
-      status_dev, dev.sms, static_cast<cudaStream_t>(stream));
+      tm_src, tm_q, M, C, expert_off, E, scales_e8m0, static_cast<long long>(Mcap), status_dev,
+      dev.sms, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }
 

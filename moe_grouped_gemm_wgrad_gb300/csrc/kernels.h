@@ -12,8 +12,9 @@ constexpr int kMaxExperts = 1024;
 
 size_t quantize_smem_bytes(int E);
 // tm_src: bf16 [M, C] source, box 128 features x 128 tokens, no swizzle.
-cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, int M, int C,
-                                  const int32_t* expert_off, int E, void* q, void* sc,
+// tm_q:   e4m3 [C, Mcap] destination, box 128 tokens x 128 features, 128B swizzle.
+cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& tm_q, int M,
+                                  int C, const int32_t* expert_off, int E, void* sc,
                                   long long Mcap, int* status, int num_sms, cudaStream_t stream);
 
 // True when grad_w tiles go to CTA pairs (tcgen05 cta_group::2); this sets the box

@@ -7,8 +7,9 @@
 // conversion of the previous unit.  Per unit every thread owns one pair of
 // adjacent features and one 32-token block: 32-bit shared-memory reads, the
 // block maximum from the bf16 bits, an exact power-of-two scale, the hardware's
-// round-to-nearest-even saturating e4m3 convert.  The e4m3 tile leaves through
-// shared memory as full 128-byte rows, the 512-byte scale atom in one piece.
+// round-to-nearest-even saturating e4m3 convert.  The e4m3 tile (128B-swizzled) and
+// its 512-byte scale atom leave through a double-buffered staging area with TMA
+// bulk stores, so the CTA goes on to the next unit while they drain.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -23,13 +24,28 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kInBytes = 128 * 128 * 2;  // bf16 tile [token][feature], 256-byte rows
 constexpr int kInStages = 2;
-constexpr int kOutPitch = 144;           // bytes per feature row of the e4m3 tile (128 + 16 pad)
-constexpr int kOutBytes = 128 * kOutPitch;
+constexpr int kOutTile = 128 * 128;      // e4m3 tile [feature][token], 128B-swizzled rows
 constexpr int kSf = 512;
+constexpr int kOutBuf = 17408;           // tile + scale atom, padded to 1024 B
 constexpr int kOffOut = kInStages * kInBytes;
-constexpr int kOffSf = kOffOut + kOutBytes;
-constexpr int kOffBar = kOffSf + kSf;
+constexpr int kOffBar = kOffOut + 2 * kOutBuf;
 constexpr int kOffTable = kOffBar + 8 * kInStages + 16;
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_1d(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gdst)),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
@@ -74,14 +90,13 @@ __device__ __forceinline__ Unit locate(int ch, int used_chunks, const int* s_off
 }
 
 __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
-    const __grid_constant__ CUtensorMap tm_src, int M, int C, const int32_t* __restrict__ expert_off,
-    int E, uint8_t* __restrict__ q, uint8_t* __restrict__ sc, long long Mcap, int* status) {
+    const __grid_constant__ CUtensorMap tm_src, const __grid_constant__ CUtensorMap tm_q, int M,
+    int C, const int32_t* __restrict__ expert_off, int E, uint8_t* __restrict__ sc, long long Mcap,
+    int* status) {
   extern __shared__ uint8_t smem_raw[];
-  // TMA destinations want 128-byte alignment; the launch adds 128 bytes of slack.
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // 128B-swizzled TMA tiles want 1024-byte alignment; the launch adds the slack.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint8_t* s_out = smem + kOffOut;
-  uint8_t* s_sf = smem + kOffSf;
   int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 8 * kInStages);  // [0] flag [1] abort
   int* s_off = reinterpret_cast<int*>(smem + kOffTable);
   int* s_pad = s_off + (E + 1);
@@ -92,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     for (int s = 0; s < kInStages; ++s) mbar_init(sbase + kOffBar + 8 * s, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_src);
+    tma_prefetch_desc(&tm_q);
   }
   if (!load_offsets(expert_off, E, M, s_off, s_pad, &s_misc[0], status)) return;
 
@@ -124,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   const int p = tid & 63;   // feature pair: features 2p, 2p+1 of the tile
   const int kb = tid >> 6;  // 32-token block of the chunk
   uint32_t phase = 0;
-  int stage = 0;
+  int stage = 0, ob = 0;
   for (long long u = blockIdx.x; u < units; u += stride) {
     const int ch = static_cast<int>(u / col_tiles);
     const int ct = static_cast<int>(u % col_tiles);
@@ -162,39 +178,40 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
                              __uint_as_float(v[i + 2] & 0xFFFF0000u) * inv_hi,
                              __uint_as_float(v[i + 3] & 0xFFFF0000u) * inv_hi);
     }
-    __syncthreads();  // every thread has read input stage `stage`; the output tile is free
+    // The store issued from this output buffer two units ago must have read it.
+    if (tid == 0) bulk_wait_read1();
+    __syncthreads();  // input stage `stage` fully read; output buffer `ob` free
     if (tid == 0) {
       const long long nu = u + kInStages * stride;
       if (nu < units) issue(nu, stage);
     }
     {
-      uint4* r0 = reinterpret_cast<uint4*>(s_out + (2 * p) * kOutPitch + kb * 32);
-      uint4* r1 = reinterpret_cast<uint4*>(s_out + (2 * p + 1) * kOutPitch + kb * 32);
-      r0[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-      r0[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-      r1[0] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-      r1[1] = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-      const int c0 = 2 * p, c1 = 2 * p + 1;
-      s_sf[(c0 & 31) * 16 + (c0 >> 5) * 4 + kb] = static_cast<uint8_t>(byte_lo);
-      s_sf[(c1 & 31) * 16 + (c1 >> 5) * 4 + kb] = static_cast<uint8_t>(byte_hi);
+      // 128 feature rows x 128 token bytes, 16-byte chunk j of row r at (j ^ (r % 8)).
+      const uint32_t obase = sbase + kOffOut + ob * kOutBuf;
+      const int r0 = 2 * p, r1 = 2 * p + 1;
+      const uint32_t a0 = obase + r0 * 128, a1 = obase + r1 * 128;
+      st_shared_v4(a0 + (((2 * kb) ^ (r0 & 7)) << 4), pl[0], pl[1], pl[2], pl[3]);
+      st_shared_v4(a0 + (((2 * kb + 1) ^ (r0 & 7)) << 4), pl[4], pl[5], pl[6], pl[7]);
+      st_shared_v4(a1 + (((2 * kb) ^ (r1 & 7)) << 4), ph[0], ph[1], ph[2], ph[3]);
+      st_shared_v4(a1 + (((2 * kb + 1) ^ (r1 & 7)) << 4), ph[4], ph[5], ph[6], ph[7]);
+      uint8_t* s_sf = smem + kOffOut + ob * kOutBuf + kOutTile;
+      s_sf[(r0 & 31) * 16 + (r0 >> 5) * 4 + kb] = static_cast<uint8_t>(byte_lo);
+      s_sf[(r1 & 31) * 16 + (r1 >> 5) * 4 + kb] = static_cast<uint8_t>(byte_hi);
     }
+    fence_async_smem();
     __syncthreads();
-    // 128 feature rows x 128 B (8 threads per row), then the 512-byte atom.
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = (tid >> 3) + i * 32, c16 = tid & 7;
-      const uint4 w = *reinterpret_cast<const uint4*>(s_out + r * kOutPitch + c16 * 16);
-      *reinterpret_cast<uint4*>(q + static_cast<size_t>(ct * 128 + r) * static_cast<size_t>(Mcap) +
-                                static_cast<size_t>(ch) * 128 + c16 * 16) = w;
+    if (tid == 0) {
+      const uint32_t obase = sbase + kOffOut + ob * kOutBuf;
+      tma_store_2d(&tm_q, ch * 128, ct * 128, obase);
+      bulk_store_1d(sc + (static_cast<size_t>(ch) * col_tiles + ct) * kSf, obase + kOutTile, kSf);
+      bulk_commit();
     }
-    if (tid < 32) {
-      const uint4 w = *reinterpret_cast<const uint4*>(s_sf + tid * 16);
-      *reinterpret_cast<uint4*>(sc + (static_cast<size_t>(ch) * col_tiles + ct) * kSf + tid * 16) = w;
-    }
+    ob ^= 1;
     if (++stage == kInStages) stage = 0, phase ^= 1u;
   }
-  // Loads issued for units this CTA never reached (only after an abort) must land
-  // before the CTA exits.
+  // All bulk stores complete before the CTA exits; loads issued for units this CTA never
+  // reached (only after an abort) must land too.
+  if (tid == 0) bulk_wait0();
   __syncthreads();
   if (tid == 0 && *abort_flag) {
     int never = 0;
@@ -205,11 +222,11 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
 }  // namespace
 
 size_t quantize_smem_bytes(int E) {
-  return static_cast<size_t>(kOffTable) + sizeof(int) * (2 * (E + 1)) + 128;
+  return static_cast<size_t>(kOffTable) + sizeof(int) * (2 * (E + 1)) + 1024;
 }
 
-cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, int M, int C,
-                                  const int32_t* expert_off, int E, void* q, void* sc,
+cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& tm_q, int M,
+                                  int C, const int32_t* expert_off, int E, void* sc,
                                   long long Mcap, int* status, int num_sms, cudaStream_t stream) {
   const size_t smem = quantize_smem_bytes(E);
   static thread_local int attr_set_device = -1;
@@ -231,7 +248,7 @@ cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, int M, int C,
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
   mxfp8_quantize_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
-      tm_src, M, C, expert_off, E, static_cast<uint8_t*>(q), static_cast<uint8_t*>(sc), Mcap, status);
+      tm_src, tm_q, M, C, expert_off, E, static_cast<uint8_t*>(sc), Mcap, status);
   return cudaGetLastError();
 }
 
