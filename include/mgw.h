@@ -46,6 +46,10 @@ typedef int mgw_status;
 
 #define MGW_MAX_EXPERTS 1024
 
+/* Scale rules of mgw_mxfp8_quantize. */
+#define MGW_SCALE_FLOOR 0    /* OCP MX: 2^(floor(log2 amax) - 8), saturate to +-448 */
+#define MGW_SCALE_CEIL_448 1 /* post-attn page's RoundUp: ceil_pow2(amax * fp32(1/448)) */
+
 /* Human-readable name of a return code (static string). */
 const char *mgw_status_string(mgw_status s);
 
@@ -75,10 +79,15 @@ size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap);
  * every block of 32 consecutive tokens of one expert (blocks restart at each
  * expert's first token and never mix experts):
  *   amax = max |v| over the block's tokens,
- *   scale = 2^s, s = clamp(floor(log2 amax) - 8, -127, 127)   (OCP MX rule;
- *           amax == 0 gives s = -127),
+ *   scale = 2^s with, for scale_rule MGW_SCALE_FLOOR,
+ *           s = clamp(floor(log2 amax) - 8, -127, 127)   (OCP MX rule; amax == 0 gives
+ *           s = -127), or, for MGW_SCALE_CEIL_448 (the post-attn page's mx8_scale),
+ *           s + 127 = clamp(biased exponent of ceil_pow2(amax * fp32(1/448)), 1, 254)
+ *           with the product rounded to fp32 as that page computes it,
  *   q = e4m3(v / scale), rounded to nearest even, |q| saturated at 448 (the
  *       post-attn page's mx8_q clamp).
+ * A 32-token block that holds no token of its expert (the padding up to the expert's
+ * next 128-token boundary) gets scale byte 0 and values 0 under either rule.
  *
  * src_bf16   device, bf16 [M, C] row-major (token-major), read only.
  * M          tokens, >= 0.  C: features, a positive multiple of 128.
@@ -92,13 +101,14 @@ size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap);
  *            token t the byte is at
  *              ((t/128) * (C/128) + c/128) * 512 + (c%32)*16 + ((c%128)/32)*4 + (t%128)/32.
  * Mcap       padded token axis, multiple of 128, >= mgw_mxfp8_token_capacity(M, E).
+ * scale_rule MGW_SCALE_FLOOR or MGW_SCALE_CEIL_448; anything else is MGW_ERR_INVALID_ARG.
  * status_dev device int, nullable.  With NULL an invalid expert_off is not
  *            reported (the kernel still writes nothing).
  * Returns MGW_OK or a negative code; no work is launched on error.
  */
 mgw_status mgw_mxfp8_quantize(const void *src_bf16, int M, int C, const int32_t *expert_off,
                               int E, void *q_e4m3, void *scales_e8m0, size_t Mcap,
-                              int *status_dev, void *stream);
+                              int scale_rule, int *status_dev, void *stream);
 
 /* ---------------------------------------------------------------- wgrad
  * mgw_grouped_wgrad_mxfp8 -- grouped expert weight gradient

@@ -109,9 +109,10 @@ size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap) {
 
 mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t* expert_off,
                               int E, void* q_e4m3, void* scales_e8m0, size_t Mcap,
-                              int* status_dev, void* stream) {
+                              int scale_rule, int* status_dev, void* stream) {
   if (!expert_off || !q_e4m3 || !scales_e8m0 || (M > 0 && !src_bf16)) return MGW_ERR_INVALID_ARG;
   if (M < 0 || C <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
+  if (scale_rule != MGW_SCALE_FLOOR && scale_rule != MGW_SCALE_CEIL_448) return MGW_ERR_INVALID_ARG;
   if (C % 128 != 0) return MGW_ERR_UNSUPPORTED;
   if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
     return MGW_ERR_CAPACITY;
@@ -131,8 +132,8 @@ mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t*
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_mxfp8_quantize(
-      tm_src, tm_q, M, C, expert_off, E, scales_e8m0, static_cast<long long>(Mcap), status_dev,
-      dev.sms, static_cast<cudaStream_t>(stream));
+      tm_src, tm_q, M, C, expert_off, E, scales_e8m0, static_cast<long long>(Mcap), scale_rule,
+      status_dev, dev.sms, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }
 

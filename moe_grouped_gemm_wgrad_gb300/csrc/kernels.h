@@ -15,7 +15,8 @@ size_t quantize_smem_bytes(int E);
 // tm_q:   e4m3 [C, Mcap] destination, box 128 tokens x 128 features, 128B swizzle.
 cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& tm_q, int M,
                                   int C, const int32_t* expert_off, int E, void* sc,
-                                  long long Mcap, int* status, int num_sms, cudaStream_t stream);
+                                  long long Mcap, int rule, int* status, int num_sms,
+                                  cudaStream_t stream);
 
 // True when grad_w tiles go to CTA pairs (tcgen05 cta_group::2); this sets the box
 // height of tm_b (128 rows for pairs, 256 otherwise) and whether tm_sfa/tm_sfb are used.

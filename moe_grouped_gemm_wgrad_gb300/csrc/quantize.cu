@@ -53,13 +53,25 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float 
   return lo | (hi << 16);
 }
 
-// floor(log2 amax) is the bf16 exponent field minus 127 for normal values; the
-// scale byte is that minus 8 plus the bias 127, clamped at 0 (which also covers
-// amax == 0 and every subnormal amax).  Returns the byte; *inv = 2^(127 - byte).
-__device__ __forceinline__ int scale_byte(uint32_t amax_bits, float* inv) {
-  const int ef = static_cast<int>(amax_bits >> 7);
-  const int byte = ef > 8 ? ef - 8 : 0;
-  *inv = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);
+// Rule 0 (OCP MX): floor(log2 amax) is the bf16 exponent field minus 127 for normal
+// values; the scale byte is that minus 8 plus the bias 127, clamped at 0 (which also
+// covers amax == 0 and every subnormal amax).
+// Rule 1 (the post-attn page's RoundUp): the biased exponent of amax * fp32(1/448)
+// rounded up to a power of two, clamped to [1, 254].
+// Returns the byte; *inv = 2^(127 - byte) (exact; subnormal for byte 254).
+__device__ __forceinline__ int scale_byte(uint32_t amax_bits, int rule, float* inv) {
+  int byte;
+  if (rule == 0) {
+    const int ef = static_cast<int>(amax_bits >> 7);
+    byte = ef > 8 ? ef - 8 : 0;
+  } else {
+    const float r = __fmul_rn(__uint_as_float(amax_bits << 16), 1.0f / 448.0f);
+    const uint32_t rb = __float_as_uint(r);
+    byte = static_cast<int>((rb >> 23) & 0xFFu) + ((rb & 0x7FFFFFu) != 0u ? 1 : 0);
+    byte = min(max(byte, 1), 254);
+  }
+  *inv = byte < 254 ? __uint_as_float(static_cast<uint32_t>(254 - byte) << 23)
+                    : __uint_as_float(0x00400000u);
   return byte;
 }
 
@@ -92,7 +104,7 @@ __device__ __forceinline__ Unit locate(int ch, int used_chunks, const int* s_off
 __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     const __grid_constant__ CUtensorMap tm_src, const __grid_constant__ CUtensorMap tm_q, int M,
     int C, const int32_t* __restrict__ expert_off, int E, uint8_t* __restrict__ sc, long long Mcap,
-    int* status) {
+    int rule, int* status) {
   extern __shared__ uint8_t smem_raw[];
   // 128B-swizzled TMA tiles want 1024-byte alignment; the launch adds the slack.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -166,8 +178,9 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
       amax_hi = max(amax_hi, (v[i] >> 16) & 0x7FFFu);
     }
     float inv_lo, inv_hi;
-    const int byte_lo = scale_byte(amax_lo, &inv_lo);
-    const int byte_hi = scale_byte(amax_hi, &inv_hi);
+    int byte_lo = scale_byte(amax_lo, rule, &inv_lo);
+    int byte_hi = scale_byte(amax_hi, rule, &inv_hi);
+    if (nvalid == 0) byte_lo = byte_hi = 0;  // a block with no token of the expert: padding
     uint32_t pl[8], ph[8];
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
@@ -227,7 +240,8 @@ size_t quantize_smem_bytes(int E) {
 
 cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& tm_q, int M,
                                   int C, const int32_t* expert_off, int E, void* sc,
-                                  long long Mcap, int* status, int num_sms, cudaStream_t stream) {
+                                  long long Mcap, int rule, int* status, int num_sms,
+                                  cudaStream_t stream) {
   const size_t smem = quantize_smem_bytes(E);
   static thread_local int attr_set_device = -1;
   int dev = 0;
@@ -248,7 +262,7 @@ cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& 
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
   mxfp8_quantize_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
-      tm_src, tm_q, M, C, expert_off, E, static_cast<uint8_t*>(sc), Mcap, status);
+      tm_src, tm_q, M, C, expert_off, E, static_cast<uint8_t*>(sc), Mcap, rule, status);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,8 @@ MGW_OK = 0
 MGW_DEV_BAD_OFFSETS = 1
 MGW_DEV_TIMEOUT = 2
 MAX_EXPERTS = 1024
+SCALE_FLOOR = 0      # OCP MX rule 2^(floor(log2 amax) - 8)
+SCALE_CEIL_448 = 1   # the post-attn page's RoundUp rule ceil_pow2(amax / 448)
 
 EXPORTS = (
     "mgw_status_string", "mgw_version", "mgw_mxfp8_token_capacity", "mgw_mxfp8_scale_bytes",
@@ -53,7 +55,7 @@ def load() -> ctypes.CDLL:
         lib.mgw_mxfp8_token_capacity.restype = SZ
         lib.mgw_mxfp8_scale_bytes.argtypes = [I, SZ]
         lib.mgw_mxfp8_scale_bytes.restype = SZ
-        lib.mgw_mxfp8_quantize.argtypes = [P, I, I, P, I, P, P, SZ, P, P]
+        lib.mgw_mxfp8_quantize.argtypes = [P, I, I, P, I, P, P, SZ, I, P, P]
         lib.mgw_mxfp8_quantize.restype = I
         lib.mgw_grouped_wgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
         lib.mgw_grouped_wgrad_mxfp8.restype = I
@@ -98,7 +100,7 @@ def scale_bytes(C: int, Mcap: int) -> int:
 
 def mxfp8_quantize(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int | None = None,
                    q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
-                   status: torch.Tensor | None = None, stream=None):
+                   status: torch.Tensor | None = None, stream=None, scale_rule: int = SCALE_FLOOR):
     """MXFP8-quantize bf16 ``src`` [M, C] along tokens -> (q uint8 [C, Mcap], scales uint8)."""
     _dev_tensor(src, torch.bfloat16, "src")
     _dev_tensor(expert_off, torch.int32, "expert_off")
@@ -111,7 +113,7 @@ def mxfp8_quantize(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int | None
     if scales is None:
         scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
     st = load().mgw_mxfp8_quantize(_ptr(src), M, C, _ptr(expert_off), E, _ptr(q), _ptr(scales),
-                                   Mcap, _ptr(status), _stream(stream))
+                                   Mcap, int(scale_rule), _ptr(status), _stream(stream))
     _check(st, "mgw_mxfp8_quantize")
     return q, scales
 

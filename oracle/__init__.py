@@ -61,9 +61,11 @@ def _load():
             lib.orc_e8m0_decode.restype = dbl
             lib.orc_mx_scale_byte.argtypes = [dbl]
             lib.orc_mx_scale_byte.restype = u8
+            lib.orc_mx_scale_byte_ceil448.argtypes = [dbl]
+            lib.orc_mx_scale_byte_ceil448.restype = u8
             lib.orc_padded_starts.argtypes = [P, i32, P]
             lib.orc_padded_starts.restype = None
-            lib.orc_mxfp8_quantize.argtypes = [P, i32, i32, P, i32, i64, P, P]
+            lib.orc_mxfp8_quantize.argtypes = [P, i32, i32, P, i32, i64, i32, P, P]
             lib.orc_mxfp8_quantize.restype = None
             lib.orc_grouped_wgrad.argtypes = [P, P, P, P, P, i32, i32, i32, i64, P]
             lib.orc_grouped_wgrad.restype = None
@@ -111,6 +113,15 @@ def mx_scale_byte(amax: float) -> int:
     return int(_load().orc_mx_scale_byte(float(amax)))
 
 
+def mx_scale_byte_ceil448(amax: float) -> int:
+    """The post-attn page's RoundUp rule: exponent of ceil_pow2(amax * fp32(1/448)), in [1, 254]."""
+    return int(_load().orc_mx_scale_byte_ceil448(float(amax)))
+
+
+SCALE_FLOOR = 0     # OCP MX rule 2^(floor(log2 amax) - 8)
+SCALE_CEIL_448 = 1  # the post-attn page's RoundUp rule
+
+
 def padded_starts(expert_off) -> np.ndarray:
     """P[e]: start of expert e's 128-padded segment in the quantized token axis."""
     off = _off(expert_off)
@@ -126,9 +137,11 @@ def token_capacity(M: int, E: int) -> int:
 
 
 # ---------------------------------------------------------------- quantize
-def mxfp8_quantize(src_bf16_bits: np.ndarray, expert_off, Mcap: int | None = None):
+def mxfp8_quantize(src_bf16_bits: np.ndarray, expert_off, Mcap: int | None = None,
+                   rule: int = SCALE_FLOOR):
     """MXFP8 quantization along the token axis (wgrad page: A = g^T, B = x^T in e4m3
-    with e8m0 scales per 32 tokens).  ``src_bf16_bits`` is uint16 [M, C].
+    with e8m0 scales per 32 tokens).  ``src_bf16_bits`` is uint16 [M, C]; ``rule`` picks
+    the scale rule (SCALE_FLOOR or SCALE_CEIL_448).
 
     Returns (q [C, Mcap] uint8, sc [C, Mcap/32] uint8) in the plain layout."""
     src = np.ascontiguousarray(src_bf16_bits, dtype=np.uint16)
@@ -139,7 +152,7 @@ def mxfp8_quantize(src_bf16_bits: np.ndarray, expert_off, Mcap: int | None = Non
         Mcap = token_capacity(M, E)
     q = np.empty((C, Mcap), dtype=np.uint8)
     sc = np.empty((C, Mcap // 32), dtype=np.uint8)
-    _load().orc_mxfp8_quantize(_ptr(src), M, C, _ptr(off), E, Mcap, _ptr(q), _ptr(sc))
+    _load().orc_mxfp8_quantize(_ptr(src), M, C, _ptr(off), E, Mcap, int(rule), _ptr(q), _ptr(sc))
     return q, sc
 
 

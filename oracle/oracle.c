@@ -75,6 +75,20 @@ uint8_t orc_mx_scale_byte(double amax) {
   return (uint8_t)(s + 127);
 }
 
+/* The post-attn page's mx8_scale: amax times the fp32 constant 1/448, rounded to fp32;
+ * the biased exponent of that product, plus one when its mantissa is not zero (rounding
+ * up to a power of two); kept within [1, 254]. */
+uint8_t orc_mx_scale_byte_ceil448(double amax) {
+  const float r = (float)amax * (1.0f / 448.0f);
+  uint32_t bits;
+  memcpy(&bits, &r, sizeof bits);
+  int e = (int)((bits >> 23) & 0xFFu);
+  if ((bits & 0x7FFFFFu) != 0) e += 1;
+  if (e > 254) e = 254;
+  if (e < 1) e = 1;
+  return (uint8_t)e;
+}
+
 double orc_bf16_decode(uint16_t h) {
   /* bf16 is the top half of an IEEE binary32; widen by placing it there. */
   const uint32_t bits = (uint32_t)h << 16;
@@ -100,9 +114,10 @@ void orc_padded_starts(const int32_t *off, int E, int64_t *P) {
  * The scale rule is the MX one, 2^(floor(log2 amax) - 8); values beyond the
  * e4m3 range after scaling are clamped to +-448 as the post-attn page's mx8_q
  * does, and rounding is to nearest even.  Blocks start at each expert's first
- * token, so no block mixes two experts. */
+ * token, so no block mixes two experts.  With rule 1 the scale follows that page's
+ * RoundUp rule instead. */
 void orc_mxfp8_quantize(const uint16_t *src, int M, int C, const int32_t *off, int E,
-                        int64_t Mcap, uint8_t *q, uint8_t *sc) {
+                        int64_t Mcap, int rule, uint8_t *q, uint8_t *sc) {
   (void)M;
   const int64_t nsc = Mcap / 32;
   memset(q, 0, (size_t)C * (size_t)Mcap);
@@ -122,7 +137,7 @@ void orc_mxfp8_quantize(const uint16_t *src, int M, int C, const int32_t *off, i
           const double v = fabs(orc_bf16_decode(src[(int64_t)(t0 + t) * C + c]));
           if (v > amax) amax = v;
         }
-        const uint8_t byte = orc_mx_scale_byte(amax);
+        const uint8_t byte = rule ? orc_mx_scale_byte_ceil448(amax) : orc_mx_scale_byte(amax);
         const int s = (int)byte - 127;
         sc[(int64_t)c * nsc + P[e] / 32 + j] = byte;
         for (int t = b0; t < b1; ++t) {

@@ -31,6 +31,10 @@ double orc_e8m0_decode(uint8_t b);
 /* MX shared-exponent rule for one block: byte of 2^(floor(log2 amax) - 8),
  * clamped to [-127, 127] before the +127 bias; amax == 0 gives byte 0. */
 uint8_t orc_mx_scale_byte(double amax);
+/* The post-attn page's RoundUp rule (its mx8_scale): byte = biased exponent of
+ * ceil_pow2(amax * fp32(1/448)), the product taken in fp32 as the page does, clamped to
+ * [1, 254].  Values are then scaled by 2^(127-byte) and clamped to +-448 (its mx8_q). */
+uint8_t orc_mx_scale_byte_ceil448(double amax);
 /* bf16 bit pattern -> exact value. */
 double orc_bf16_decode(uint16_t h);
 
@@ -43,8 +47,10 @@ void orc_padded_starts(const int32_t *off, int E, int64_t *P);
  *   q  : [C, Mcap] e4m3 bytes, token-contiguous, expert e at P[e]; pads 0.
  *   sc : [C, Mcap/32] e8m0 bytes (plain layout), block j of expert e at
  *        P[e]/32 + j; pads 0. */
+/* rule 0: the MX floor rule (orc_mx_scale_byte); rule 1: the RoundUp rule
+ * (orc_mx_scale_byte_ceil448). */
 void orc_mxfp8_quantize(const uint16_t *src, int M, int C, const int32_t *off, int E,
-                        int64_t Mcap, uint8_t *q, uint8_t *sc);
+                        int64_t Mcap, int rule, uint8_t *q, uint8_t *sc);
 
 /* Grouped wgrad: out[(e*N+n)*K + k] = sum_{t<cnt_e} deq(g)[n, P_e+t] * deq(x)[k, P_e+t]
  * in fp64, from the quantized operands (q and plain scales as above). */

@@ -45,15 +45,17 @@ def test_argument_errors_before_device_work(lib):
     P = ctypes.c_void_p
     fake = P(0x1000)  # never dereferenced: validation fails first
     # null pointers
-    assert lib.mgw_mxfp8_quantize(fake, 4, 128, None, 1, fake, fake, 256, None, None) == -1
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, None, 1, fake, fake, 256, 0, None, None) == -1
     # C not a multiple of 128
-    assert lib.mgw_mxfp8_quantize(fake, 4, 96, fake, 1, fake, fake, 256, None, None) == -2
+    assert lib.mgw_mxfp8_quantize(fake, 4, 96, fake, 1, fake, fake, 256, 0, None, None) == -2
     # Mcap too small / not a multiple of 128
-    assert lib.mgw_mxfp8_quantize(fake, 300, 128, fake, 2, fake, fake, 384, None, None) == -3
-    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1, fake, fake, 200, None, None) == -3
+    assert lib.mgw_mxfp8_quantize(fake, 300, 128, fake, 2, fake, fake, 384, 0, None, None) == -3
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1, fake, fake, 200, 0, None, None) == -3
+    # unknown scale rule
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1, fake, fake, 256, 7, None, None) == -1
     # E out of range
-    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 0, fake, fake, 256, None, None) == -1
-    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1025, fake, fake, 1 << 20, None, None) == -1
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 0, fake, fake, 256, 0, None, None) == -1
+    assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1025, fake, fake, 1 << 20, 0, None, None) == -1
     # wgrad: K not a multiple of 256, N not a multiple of 128
     assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, fake, None, None) == -2
     assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 64, 256, 256, fake, None, None) == -2

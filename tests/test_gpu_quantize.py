@@ -104,3 +104,19 @@ def test_quantize_max_experts():
     counts = np.where(rng.random(1024) < 0.2, rng.integers(1, 70, 1024), 0)
     case = synth.wgrad_random(int(counts.sum()), 256, 128, counts, seed=45)
     _check(case.g_bf16, case.expert_off)
+
+
+@pytest.mark.parametrize("counts,C", [([128, 128], 256), ([0, 33, 128, 1, 0, 200], 128),
+                                      ([31, 32, 33, 127, 129], 128)])
+def test_quantize_ceil448_rule_matches_oracle(counts, C):
+    case = synth.wgrad_random(sum(counts), C, 128, counts, seed=sum(counts) + 7, outlier_frac=0.02)
+    M, E = sum(counts), len(counts)
+    Mcap = mgw.token_capacity(M, E)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, sc = mgw.mxfp8_quantize(dev_bf16(case.g_bf16), dev_i32(case.expert_off), Mcap=Mcap,
+                               status=status, scale_rule=mgw.SCALE_CEIL_448)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    oq, osc = oracle.mxfp8_quantize(case.g_bf16, case.expert_off, Mcap, rule=oracle.SCALE_CEIL_448)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(atoms_to_plain(sc.cpu().numpy(), C, Mcap), osc)

@@ -160,3 +160,20 @@ def test_wgrad_device_time_limit_reports_and_context_survives(monkeypatch):
     assert int(status.item()) & mgw.MGW_DEV_TIMEOUT
     monkeypatch.delenv("MGW_TEST_DROP_LOAD")
     _check_full(case)
+
+
+def test_wgrad_from_ceil448_operands():
+    """The wgrad consumes operands quantized with the RoundUp scale rule just the same."""
+    case = synth.wgrad_random(463, 256, 512, [0, 1, 129, 300, 33], seed=47, outlier_frac=0.01)
+    off = dev_i32(case.expert_off)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rule = mgw.SCALE_CEIL_448
+    gq, gs = mgw.mxfp8_quantize(dev_bf16(case.g_bf16), off, status=status, scale_rule=rule)
+    xq, xs = mgw.mxfp8_quantize(dev_bf16(case.x_bf16), off, status=status, scale_rule=rule)
+    out = bf16_to_f64(mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, case.M, status=status))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ogq, ogs = oracle.mxfp8_quantize(case.g_bf16, case.expert_off, rule=oracle.SCALE_CEIL_448)
+    oxq, oxs = oracle.mxfp8_quantize(case.x_bf16, case.expert_off, rule=oracle.SCALE_CEIL_448)
+    ref = oracle.grouped_wgrad(ogq, ogs, oxq, oxs, case.expert_off)
+    assert np.all(np.abs(out - ref) <= wgrad_tol(ref))

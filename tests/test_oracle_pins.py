@@ -255,3 +255,39 @@ def test_dgrad_single_expert_is_dense_gemm():
     dx, _ = oracle.grouped_dgrad(case.dy, case.W, case.expert_off)
     np.testing.assert_allclose(dx, case.dy.astype(np.float64) @ case.W[0].astype(np.float64),
                                rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ RoundUp scale rule
+def test_ceil448_scale_golden_and_bracket():
+    g = _golden("e4m3_e8m0_examples.json")["scale_byte_ceil448"]
+    for ex in g["examples"]:
+        assert oracle.mx_scale_byte_ceil448(ex["amax"]) == ex["byte"], ex
+    rng = np.random.default_rng(6)
+    for amax in np.exp2(rng.uniform(-30, 30, 500)):
+        amax = float(np.float32(amax))
+        b = oracle.mx_scale_byte_ceil448(amax)
+        assert 1 <= b <= 254
+        # the power of two is the smallest with 448 * 2^(b-127) >= amax, up to fp32 rounding
+        assert 448.0 * 2.0 ** (b - 127) >= amax * (1 - 2.0 ** -22)
+        assert 448.0 * 2.0 ** (b - 128) < amax * (1 + 2.0 ** -22)
+
+
+def test_quantize_ceil448_never_saturates_and_rounds_to_nearest():
+    counts = [40, 0, 97]
+    case = synth.wgrad_random(sum(counts), 16, 16, counts, seed=12, outlier_frac=0.05)
+    q, sc = oracle.mxfp8_quantize(case.g_bf16, case.expert_off, rule=oracle.SCALE_CEIL_448)
+    P = oracle.padded_starts(case.expert_off)
+    v = synth.bf16_bits_to_f32(case.g_bf16).astype(np.float64)
+    deq = _torch_deq(q, sc)
+    off = case.expert_off
+    for e, cnt in enumerate(counts):
+        if not cnt:
+            continue
+        seg = deq[:, P[e]:P[e] + cnt].T
+        src = v[off[e]:off[e + 1]]
+        s = np.ldexp(1.0, np.repeat(sc[:, P[e] // 32:P[e] // 32 + (cnt + 31) // 32].astype(int) - 127, 32, axis=1)[:, :cnt].T)
+        assert np.all(np.abs(src) <= 448 * s * (1 + 2.0 ** -22))  # no value beyond the range
+        err = np.abs(seg - src)
+        assert np.all(err <= np.maximum(np.abs(src) * 2.0 ** -4, s * 2.0 ** -10))
+        # the padding blocks of the segment keep byte 0
+        assert not sc[:, (P[e] + cnt + 31) // 32:P[e + 1] // 32].any()
