@@ -151,6 +151,11 @@ def run_wgrad(name, steps, warmup, dist_ctx):
     g_host = torch.from_numpy(case.g_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_host = torch.from_numpy(case.x_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
     off_host = torch.from_numpy(case.expert_off).pin_memory()
+    gather = "hidden_bf16" in case.meta  # x = hidden[token_of_row]: quantize by gather
+    if gather:
+        x_host = torch.from_numpy(case.meta["hidden_bf16"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        rows_host = torch.from_numpy(case.meta["token_of_row"]).pin_memory()
+        rows_dev = rows_host.to(dev)
     g = g_host.to(dev)
     x = x_host.to(dev)
     off = off_host.to(dev)
@@ -162,9 +167,15 @@ def run_wgrad(name, steps, warmup, dist_ctx):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
+    def quant_x():
+        if gather:
+            mgw.mxfp8_quantize_gather(x, rows_dev, off, Mcap, xq, xs, status)
+        else:
+            mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)
+
     def step():
         mgw.mxfp8_quantize(g, off, Mcap, gq, gs, status)
-        mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)
+        quant_x()
         mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
 
     clocks = ClockSampler(dist_ctx.local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_r{dist_ctx.rank}.csv")
@@ -184,7 +195,7 @@ def run_wgrad(name, steps, warmup, dist_ctx):
         ev[i][0].record(stream)
         mgw.mxfp8_quantize(g, off, Mcap, gq, gs, status)
         ev[i][1].record(stream)
-        mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)
+        quant_x()
         ev[i][2].record(stream)
         mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
         ev[i][3].record(stream)
@@ -208,6 +219,8 @@ def run_wgrad(name, steps, warmup, dist_ctx):
         g.copy_(g_host, non_blocking=True)
         x.copy_(x_host, non_blocking=True)
         off.copy_(off_host, non_blocking=True)
+        if gather:
+            rows_dev.copy_(rows_host, non_blocking=True)
         step()
         out_host.copy_(out, non_blocking=True)
 
@@ -221,17 +234,19 @@ def run_wgrad(name, steps, warmup, dist_ctx):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = dist_ctx.max(a.elapsed_time(b)) / e2e_steps
-    h2d = g_host.numel() * 2 + x_host.numel() * 2 + off_host.numel() * 4
+    h2d = g_host.numel() * 2 + x_host.numel() * 2 + off_host.numel() * 4 + (rows_host.numel() * 4 if gather else 0)
     d2h = out_host.numel() * 2
 
     ms_step = total_ms / steps
     wg_avg = statistics.mean(wg_ms)
     bytes_q = lambda C: M * C * 2 + C * Mcap + C * Mcap // 32  # noqa: E731
+    # gathered x reads each source row once per routed copy (HBM once, the rest from L2);
+    # the bytes counted here are the routed rows, as for the materialised operand
     return {
         "case": case, "flops": flops, "ms_per_step": ms_step, "wgrad_ms": wg_avg,
         "wgrad_ms_median": statistics.median(wg_ms), "quant_g_ms": statistics.mean(qg_ms),
         "quant_x_ms": statistics.mean(qx_ms), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-        "clocks": clk, "launches": 3 * steps,
+        "clocks": clk, "launches": 3 * steps, "x_gather": gather,
         "quant_bytes": bytes_q(N) + bytes_q(K),
         "wgrad_min_bytes": N * Mcap + K * Mcap + (N + K) * Mcap // 32 + E * N * K * 2,
     }
@@ -416,7 +431,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp8-e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
             "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "experts": case.E,
-                       "step": "mxfp8_quantize(g) + mxfp8_quantize(x) + grouped_wgrad_mxfp8",
+                       "step": ("mxfp8_quantize(g) + mxfp8_quantize_gather(hidden, token_of_row) + grouped_wgrad_mxfp8"
+                                if r["x_gather"] else "mxfp8_quantize(g) + mxfp8_quantize(x) + grouped_wgrad_mxfp8"),
                        "l2": "inputs larger than L2 (bf16 g,x 2x134 MB; grad_w 1.07 GB per step)",
                        "parallelism": f"replicas x{d.world} (independent workloads, no collective)"},
             "roofline": {"bound": "tensor", "achieved": wg_tflops, "peak": mxfp8_peak,

@@ -43,6 +43,7 @@ typedef int mgw_status;
 /* Bits OR-ed into *status_dev by the kernels (the caller zeroes it). */
 #define MGW_DEV_BAD_OFFSETS 1 /* expert_off[0] != 0, decreasing, or expert_off[E] != M/rows */
 #define MGW_DEV_TIMEOUT 2     /* an internal pipeline wait exceeded 1 s; outputs undefined */
+#define MGW_DEV_BAD_INDEX 4   /* mgw_mxfp8_quantize_gather: a row index outside the source */
 
 #define MGW_MAX_EXPERTS 1024
 
@@ -109,6 +110,25 @@ size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap);
 mgw_status mgw_mxfp8_quantize(const void *src_bf16, int M, int C, const int32_t *expert_off,
                               int E, void *q_e4m3, void *scales_e8m0, size_t Mcap,
                               int scale_rule, int *status_dev, void *stream);
+
+/* mgw_mxfp8_quantize_gather -- the same quantization of the routed token matrix
+ * x[t, :] = src[row_index[t], :] without materialising it.  In an MoE layer the routed
+ * rows of one expert are copies of rows of the token (hidden-state) matrix; the
+ * post-attn page's wide MoE path builds such per-expert row tables (its down_tables)
+ * for the same gather.
+ *
+ * src_bf16   device, bf16 [src_rows, C] row-major (the unpermuted token matrix).
+ * src_rows   rows of src, >= 1 when M > 0.
+ * row_index  device int32 [M]: routed token t reads source row row_index[t].  An index
+ *            outside [0, src_rows) is not read: that row is quantized as zeros and
+ *            MGW_DEV_BAD_INDEX is set in *status_dev.
+ * Every other argument, the output layout and the errors are those of
+ * mgw_mxfp8_quantize. */
+mgw_status mgw_mxfp8_quantize_gather(const void *src_bf16, int src_rows,
+                                     const int32_t *row_index, int M, int C,
+                                     const int32_t *expert_off, int E, void *q_e4m3,
+                                     void *scales_e8m0, size_t Mcap, int scale_rule,
+                                     int *status_dev, void *stream);
 
 /* ---------------------------------------------------------------- wgrad
  * mgw_grouped_wgrad_mxfp8 -- grouped expert weight gradient

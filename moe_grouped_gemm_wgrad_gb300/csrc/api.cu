@@ -107,12 +107,18 @@ size_t mgw_mxfp8_scale_bytes(int C, size_t Mcap) {
   return static_cast<size_t>(C) * Mcap / 32u;
 }
 
-mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t* expert_off,
-                              int E, void* q_e4m3, void* scales_e8m0, size_t Mcap,
-                              int scale_rule, int* status_dev, void* stream) {
+}  // extern "C"
+
+namespace {
+
+mgw_status quantize_impl(const void* src_bf16, int src_rows, const int32_t* row_index, int M,
+                         int C, const int32_t* expert_off, int E, void* q_e4m3,
+                         void* scales_e8m0, size_t Mcap, int scale_rule, int* status_dev,
+                         void* stream) {
   if (!expert_off || !q_e4m3 || !scales_e8m0 || (M > 0 && !src_bf16)) return MGW_ERR_INVALID_ARG;
   if (M < 0 || C <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
   if (scale_rule != MGW_SCALE_FLOOR && scale_rule != MGW_SCALE_CEIL_448) return MGW_ERR_INVALID_ARG;
+  if (row_index != nullptr && src_rows < 1) return MGW_ERR_INVALID_ARG;
   if (C % 128 != 0) return MGW_ERR_UNSUPPORTED;
   if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
     return MGW_ERR_CAPACITY;
@@ -121,11 +127,16 @@ mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t*
   DeviceInfo dev;
   mgw_status st = current_device(&dev);
   if (st != MGW_OK) return st;
-  // With M == 0 no tile is ever loaded; the map then only needs a valid address.
+  // Contiguous source: 128 x 128 tiles.  Gathered source: one-row boxes for tile::gather4.
+  // With M == 0 the map is never used; it then only needs a valid address.
   CUtensorMap tm_src;
-  if (!make_map_2d(&tm_src, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M > 0 ? src_bf16 : q_e4m3, C,
-                   M > 0 ? static_cast<uint64_t>(M) : 1, static_cast<uint64_t>(C) * 2, 128, 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+  const bool gather = M > 0 && row_index != nullptr;
+  const bool tile_src = M > 0 && row_index == nullptr;
+  const void* map_base = (gather || tile_src) ? src_bf16 : q_e4m3;
+  const uint64_t map_rows = gather ? static_cast<uint64_t>(src_rows)
+                                   : (tile_src ? static_cast<uint64_t>(M) : 1);
+  if (!make_map_2d(&tm_src, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map_base, C, map_rows,
+                   static_cast<uint64_t>(C) * 2, 128, gather ? 1 : 128, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MGW_ERR_CUDA;
   CUtensorMap tm_q;
   if (!make_map_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_e4m3, Mcap, C, Mcap, 128, 128,
@@ -133,8 +144,29 @@ mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t*
     return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_mxfp8_quantize(
       tm_src, tm_q, M, C, expert_off, E, scales_e8m0, static_cast<long long>(Mcap), scale_rule,
-      status_dev, dev.sms, static_cast<cudaStream_t>(stream));
+      status_dev, dev.sms, static_cast<cudaStream_t>(stream), src_bf16, row_index, src_rows);
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mgw_status mgw_mxfp8_quantize(const void* src_bf16, int M, int C, const int32_t* expert_off,
+                              int E, void* q_e4m3, void* scales_e8m0, size_t Mcap,
+                              int scale_rule, int* status_dev, void* stream) {
+  return quantize_impl(src_bf16, M, nullptr, M, C, expert_off, E, q_e4m3, scales_e8m0, Mcap,
+                       scale_rule, status_dev, stream);
+}
+
+mgw_status mgw_mxfp8_quantize_gather(const void* src_bf16, int src_rows,
+                                     const int32_t* row_index, int M, int C,
+                                     const int32_t* expert_off, int E, void* q_e4m3,
+                                     void* scales_e8m0, size_t Mcap, int scale_rule,
+                                     int* status_dev, void* stream) {
+  if (M > 0 && (!row_index || !src_bf16 || src_rows < 1)) return MGW_ERR_INVALID_ARG;
+  return quantize_impl(src_bf16, src_rows, M > 0 ? row_index : nullptr, M, C, expert_off, E,
+                       q_e4m3, scales_e8m0, Mcap, scale_rule, status_dev, stream);
 }
 
 mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* xq,

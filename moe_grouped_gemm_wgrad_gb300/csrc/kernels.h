@@ -13,10 +13,13 @@ constexpr int kMaxExperts = 1024;
 size_t quantize_smem_bytes(int E);
 // tm_src: bf16 [M, C] source, box 128 features x 128 tokens, no swizzle.
 // tm_q:   e4m3 [C, Mcap] destination, box 128 tokens x 128 features, 128B swizzle.
+// With row_index != nullptr the source rows are gathered: token t reads row
+// row_index[t] of gsrc [src_rows, C] (tm_src is then unused).
 cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& tm_q, int M,
                                   int C, const int32_t* expert_off, int E, void* sc,
                                   long long Mcap, int rule, int* status, int num_sms,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const void* gsrc = nullptr,
+                                  const int32_t* row_index = nullptr, int src_rows = 0);
 
 // True when grad_w tiles go to CTA pairs (tcgen05 cta_group::2); this sets the box
 // height of tm_b (128 rows for pairs, 256 otherwise) and whether tm_sfa/tm_sfb are used.

@@ -10,6 +10,7 @@ namespace mgw {
 // Device status bits (OR-ed into the caller's status word).
 constexpr int kDevBadOffsets = 1;  // expert_off not 0 .. M, or decreasing
 constexpr int kDevTimeout = 2;     // a pipeline wait exceeded its time limit
+constexpr int kDevBadIndex = 4;    // a gather row index outside the source rows
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -101,10 +101,16 @@ __device__ __forceinline__ Unit locate(int ch, int used_chunks, const int* s_off
   return u;
 }
 
+// kGather: token row t of the [M, C] source is row row_index[t] of the unpermuted token
+// matrix [src_rows, C] (tm_src then has a one-row box); rows arrive four at a time with
+// tile::gather4 TMA loads.  Otherwise the source is contiguous and each unit's rows
+// arrive as one TMA tile.
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     const __grid_constant__ CUtensorMap tm_src, const __grid_constant__ CUtensorMap tm_q, int M,
     int C, const int32_t* __restrict__ expert_off, int E, uint8_t* __restrict__ sc, long long Mcap,
-    int rule, int* status) {
+    int rule, int* status, const uint16_t* __restrict__ gsrc, const int32_t* __restrict__ row_index,
+    int src_rows) {
   extern __shared__ uint8_t smem_raw[];
   // 128B-swizzled TMA tiles want 1024-byte alignment; the launch adds the slack.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,24 +134,80 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   const int used_chunks = s_pad[E] / 128;
   const long long stride = gridDim.x;
 
-  // Issue the TMA load of unit u into input stage s (rows past the expert are read but
-  // masked; rows past M come back as zeros).  Padding-only units load nothing.
-  auto issue = [&](long long u, int s) {
+  // Loads of unit u into input stage s, issued by warp 0 in two halves so that the
+  // gather indices can be fetched early: prep() resolves the unit (and, for a gathered
+  // source, loads its row indices into registers), fire() issues the copies.
+  // Contiguous: one TMA tile (rows past the expert are read but masked; rows past M come
+  // back as zeros).  Gather: lane l brings rows 4l .. 4l+3 with one tile::gather4 TMA;
+  // indices outside [0, src_rows) and rows past the expert's last token are passed as
+  // row -1, an out-of-bounds coordinate the TMA fills with zeros (bad indices also set
+  // kDevBadIndex).  Padding-only units load nothing.
+  const uint32_t lane = lane_id();
+  struct Pending {
+    int ct, valid, bad;
+    int rr[4];
+  };
+  auto prep = [&](long long u) {
+    Pending pd;
     const int ch = static_cast<int>(u / col_tiles);
-    const int ct = static_cast<int>(u % col_tiles);
+    pd.ct = static_cast<int>(u % col_tiles);
     const Unit un = locate(ch, used_chunks, s_off, s_pad, E);
+    pd.valid = un.valid;
+    pd.bad = 0;
+    pd.rr[0] = un.row0;
+    if (kGather) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = 4 * static_cast<int>(lane) + j;
+        int idx = -1;
+        if (r < un.valid) {
+          idx = row_index[un.row0 + r];
+          if (idx < 0 || idx >= src_rows) {
+            idx = -1;
+            pd.bad = 1;
+          }
+        }
+        pd.rr[j] = idx;
+      }
+    }
+    return pd;
+  };
+  auto fire = [&](const Pending& pd, int s) {
     const uint32_t bar = sbase + kOffBar + 8 * s;
-    if (un.valid > 0) {
-      mbar_arrive_expect_tx(bar, kInBytes);
-      tma_load_2d(sbase + s * kInBytes, &tm_src, ct * 128, un.row0, bar);
-    } else {
-      mbar_arrive(bar);
+    if (!kGather) {
+      if (lane != 0) return;
+      if (pd.valid > 0) {
+        mbar_arrive_expect_tx(bar, kInBytes);
+        tma_load_2d(sbase + s * kInBytes, &tm_src, pd.ct * 128, pd.rr[0], bar);
+      } else {
+        mbar_arrive(bar);
+      }
+      return;
+    }
+    if (pd.valid <= 0) {
+      if (lane == 0) mbar_arrive(bar);
+      return;
+    }
+    const int groups = (pd.valid + 3) >> 2;
+    const int bad = __any_sync(0xffffffffu, pd.bad);
+    if (lane == 0) {
+      if (bad && status) atomicOr(status, kDevBadIndex);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(groups) * 1024u);
+    }
+    __syncwarp();
+    if (static_cast<int>(lane) < groups) {
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(sbase + s * kInBytes + lane * 1024u),
+          "l"(reinterpret_cast<uint64_t>(&tm_src)), "r"(pd.ct * 128), "r"(pd.rr[0]), "r"(pd.rr[1]),
+          "r"(pd.rr[2]), "r"(pd.rr[3]), "r"(bar)
+          : "memory");
     }
   };
-  if (tid == 0) {
+  if (tid < 32) {
     for (int s = 0; s < kInStages; ++s) {
       const long long u = blockIdx.x + s * stride;
-      if (u < units) issue(u, s);
+      if (u < units) fire(prep(u), s);
     }
   }
 
@@ -167,6 +229,10 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
       }
       break;
     }
+    // the unit that will refill this stage: resolve it (and load its indices) now
+    const long long nu = u + kInStages * stride;
+    Pending next{0, 0, 0, {0, 0, 0, 0}};
+    if (tid < 32 && nu < units) next = prep(nu);
     const uint32_t* in = reinterpret_cast<const uint32_t*>(smem + stage * kInBytes);
     uint32_t v[32];
     uint32_t amax_lo = 0, amax_hi = 0;
@@ -194,10 +260,7 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     // The store issued from this output buffer two units ago must have read it.
     if (tid == 0) bulk_wait_read1();
     __syncthreads();  // input stage `stage` fully read; output buffer `ob` free
-    if (tid == 0) {
-      const long long nu = u + kInStages * stride;
-      if (nu < units) issue(nu, stage);
-    }
+    if (tid < 32 && nu < units) fire(next, stage);
     {
       // 128 feature rows x 128 token bytes, 16-byte chunk j of row r at (j ^ (r % 8)).
       const uint32_t obase = sbase + kOffOut + ob * kOutBuf;
@@ -241,28 +304,34 @@ size_t quantize_smem_bytes(int E) {
 cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& tm_q, int M,
                                   int C, const int32_t* expert_off, int E, void* sc,
                                   long long Mcap, int rule, int* status, int num_sms,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const void* gsrc,
+                                  const int32_t* row_index, int src_rows) {
   const size_t smem = quantize_smem_bytes(E);
   static thread_local int attr_set_device = -1;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (attr_set_device != dev) {
-    err = cudaFuncSetAttribute(mxfp8_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(quantize_smem_bytes(kMaxExperts)));
-    if (err != cudaSuccess) return err;
+    for (auto fn : {mxfp8_quantize_kernel<false>, mxfp8_quantize_kernel<true>}) {
+      err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(quantize_smem_bytes(kMaxExperts)));
+      if (err != cudaSuccess) return err;
+    }
     attr_set_device = dev;
   }
+  const bool gather = row_index != nullptr;
+  auto kernel = gather ? mxfp8_quantize_kernel<true> : mxfp8_quantize_kernel<false>;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_quantize_kernel, kThreads, smem);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const long long units = (Mcap / 128) * (C / 128);
   long long grid = static_cast<long long>(num_sms) * per_sm;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  mxfp8_quantize_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
-      tm_src, tm_q, M, C, expert_off, E, static_cast<uint8_t*>(sc), Mcap, rule, status);
+  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
+      tm_src, tm_q, M, C, expert_off, E, static_cast<uint8_t*>(sc), Mcap, rule, status,
+      static_cast<const uint16_t*>(gsrc), row_index, src_rows);
   return cudaGetLastError();
 }
 

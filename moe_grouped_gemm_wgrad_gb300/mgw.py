@@ -19,13 +19,15 @@ LIB_PATH = os.path.join(HERE, "libmgw.so")
 MGW_OK = 0
 MGW_DEV_BAD_OFFSETS = 1
 MGW_DEV_TIMEOUT = 2
+MGW_DEV_BAD_INDEX = 4
 MAX_EXPERTS = 1024
 SCALE_FLOOR = 0      # OCP MX rule 2^(floor(log2 amax) - 8)
 SCALE_CEIL_448 = 1   # the post-attn page's RoundUp rule ceil_pow2(amax / 448)
 
 EXPORTS = (
     "mgw_status_string", "mgw_version", "mgw_mxfp8_token_capacity", "mgw_mxfp8_scale_bytes",
-    "mgw_mxfp8_quantize", "mgw_grouped_wgrad_mxfp8", "mgw_grouped_dgrad_f32",
+    "mgw_mxfp8_quantize", "mgw_mxfp8_quantize_gather", "mgw_grouped_wgrad_mxfp8",
+    "mgw_grouped_dgrad_f32",
 )
 
 
@@ -57,6 +59,8 @@ def load() -> ctypes.CDLL:
         lib.mgw_mxfp8_scale_bytes.restype = SZ
         lib.mgw_mxfp8_quantize.argtypes = [P, I, I, P, I, P, P, SZ, I, P, P]
         lib.mgw_mxfp8_quantize.restype = I
+        lib.mgw_mxfp8_quantize_gather.argtypes = [P, I, P, I, I, P, I, P, P, SZ, I, P, P]
+        lib.mgw_mxfp8_quantize_gather.restype = I
         lib.mgw_grouped_wgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
         lib.mgw_grouped_wgrad_mxfp8.restype = I
         lib.mgw_grouped_dgrad_f32.argtypes = [P, P, P, I, I, I, I, P, P, P]
@@ -115,6 +119,31 @@ def mxfp8_quantize(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int | None
     st = load().mgw_mxfp8_quantize(_ptr(src), M, C, _ptr(expert_off), E, _ptr(q), _ptr(scales),
                                    Mcap, int(scale_rule), _ptr(status), _stream(stream))
     _check(st, "mgw_mxfp8_quantize")
+    return q, scales
+
+
+def mxfp8_quantize_gather(src: torch.Tensor, row_index: torch.Tensor, expert_off: torch.Tensor,
+                          Mcap: int | None = None, q: torch.Tensor | None = None,
+                          scales: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                          stream=None, scale_rule: int = SCALE_FLOOR):
+    """MXFP8-quantize the routed rows src[row_index] (src bf16 [rows, C], row_index int32 [M])
+    without materialising them -> (q uint8 [C, Mcap], scales uint8)."""
+    _dev_tensor(src, torch.bfloat16, "src")
+    _dev_tensor(row_index, torch.int32, "row_index")
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    src_rows, C = src.shape
+    M = row_index.numel()
+    E = expert_off.numel() - 1
+    if Mcap is None:
+        Mcap = token_capacity(M, E)
+    if q is None:
+        q = torch.empty((C, Mcap), dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
+    st = load().mgw_mxfp8_quantize_gather(_ptr(src), src_rows, _ptr(row_index), M, C,
+                                          _ptr(expert_off), E, _ptr(q), _ptr(scales), Mcap,
+                                          int(scale_rule), _ptr(status), _stream(stream))
+    _check(st, "mgw_mxfp8_quantize_gather")
     return q, scales
 
 

@@ -166,8 +166,11 @@ def moe_ffn_pair(seed: int = 0, tokens: int = 8192, E: int = 64, hidden: int = 4
     dy = normal_f32(rng, (rows, ffn))
     W = normal_f32(rng, (E, ffn, hidden), std=ffn ** -0.5)
     off = offsets_from_counts(counts)
+    hidden_bf16 = bf16_bits_from_f32(hidden_states)
     wg = WgradCase("moe_ffn_pair.wgrad", rows, ffn, hidden, E, off, bf16_bits_from_f32(dy),
-                   bf16_bits_from_f32(hidden_states[token_of_row]), {"counts": counts.tolist()})
+                   hidden_bf16[token_of_row],
+                   {"counts": counts.tolist(), "hidden_bf16": hidden_bf16,
+                    "token_of_row": token_of_row.astype(np.int32)})
     dg = DgradCase("moe_ffn_pair.dgrad", rows, ffn, hidden, E, off, dy, W,
                    {"counts": counts.tolist()})
     return wg, dg

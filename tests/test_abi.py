@@ -56,6 +56,11 @@ def test_argument_errors_before_device_work(lib):
     # E out of range
     assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 0, fake, fake, 256, 0, None, None) == -1
     assert lib.mgw_mxfp8_quantize(fake, 4, 128, fake, 1025, fake, fake, 1 << 20, 0, None, None) == -1
+    # gather: missing row index / source, bad scale rule, C not a multiple of 128
+    assert lib.mgw_mxfp8_quantize_gather(fake, 10, None, 4, 128, fake, 1, fake, fake, 256, 0, None, None) == -1
+    assert lib.mgw_mxfp8_quantize_gather(fake, 0, fake, 4, 128, fake, 1, fake, fake, 256, 0, None, None) == -1
+    assert lib.mgw_mxfp8_quantize_gather(fake, 10, fake, 4, 128, fake, 1, fake, fake, 256, 3, None, None) == -1
+    assert lib.mgw_mxfp8_quantize_gather(fake, 10, fake, 4, 64, fake, 1, fake, fake, 256, 0, None, None) == -2
     # wgrad: K not a multiple of 256, N not a multiple of 128
     assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, fake, None, None) == -2
     assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 64, 256, 256, fake, None, None) == -2

@@ -83,6 +83,17 @@ def test_quantize_full_size_workloads(name):
     case = synth.moe_ffn_pair()[0] if name == "moe_ffn_pair" else getattr(synth, name)()
     _check(case.g_bf16, case.expert_off)
     _check(case.x_bf16, case.expert_off)
+    if "hidden_bf16" in case.meta:  # x gathered from the hidden states by the routing map
+        Mcap = mgw.token_capacity(case.M, case.E)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q, sc = mgw.mxfp8_quantize_gather(dev_bf16(case.meta["hidden_bf16"]),
+                                          dev_i32(case.meta["token_of_row"]),
+                                          dev_i32(case.expert_off), Mcap=Mcap, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        oq, osc = oracle.mxfp8_quantize(case.x_bf16, case.expert_off, Mcap)
+        assert np.array_equal(q.cpu().numpy(), oq)
+        assert np.array_equal(atoms_to_plain(sc.cpu().numpy(), case.K, Mcap), osc)
 
 
 def test_quantize_bad_offsets_reported_and_output_untouched():
@@ -120,3 +131,52 @@ def test_quantize_ceil448_rule_matches_oracle(counts, C):
     oq, osc = oracle.mxfp8_quantize(case.g_bf16, case.expert_off, Mcap, rule=oracle.SCALE_CEIL_448)
     assert np.array_equal(q.cpu().numpy(), oq)
     assert np.array_equal(atoms_to_plain(sc.cpu().numpy(), C, Mcap), osc)
+
+
+def _routed_case(tokens, C, E, top_k, seed):
+    token_of_row, counts = synth.moe_routing(seed, tokens, E, top_k)
+    rng = np.random.default_rng(seed + 100)
+    hidden = synth.bf16_bits_from_f32(synth.normal_f32(rng, (tokens, C)))
+    return hidden, token_of_row.astype(np.int32), synth.offsets_from_counts(counts)
+
+
+@pytest.mark.parametrize("tokens,C,E,top_k", [(300, 256, 8, 2), (1000, 128, 16, 4), (64, 384, 3, 3)])
+def test_quantize_gather_matches_oracle_on_routed_rows(tokens, C, E, top_k):
+    hidden, rows, off = _routed_case(tokens, C, E, top_k, seed=tokens + C)
+    M = rows.size
+    Mcap = mgw.token_capacity(M, E)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, sc = mgw.mxfp8_quantize_gather(dev_bf16(hidden), dev_i32(rows), dev_i32(off), Mcap=Mcap,
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    oq, osc = oracle.mxfp8_quantize(np.ascontiguousarray(hidden[rows]), off, Mcap)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(atoms_to_plain(sc.cpu().numpy(), C, Mcap), osc)
+
+
+def test_quantize_gather_bad_indices_zero_rows_and_status():
+    hidden, rows, off = _routed_case(200, 128, 4, 2, seed=5)
+    bad = rows.copy()
+    bad[[0, 17, 250]] = [-1, 200, 10 ** 6]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M = rows.size
+    Mcap = mgw.token_capacity(M, 4)
+    q, sc = mgw.mxfp8_quantize_gather(dev_bf16(hidden), dev_i32(bad), dev_i32(off), Mcap=Mcap,
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & mgw.MGW_DEV_BAD_INDEX
+    src = np.ascontiguousarray(hidden[np.clip(bad, 0, 199)])
+    src[[0, 17, 250]] = 0
+    oq, osc = oracle.mxfp8_quantize(src, off, Mcap)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(atoms_to_plain(sc.cpu().numpy(), 128, Mcap), osc)
+
+
+def test_quantize_gather_no_tokens():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hidden = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
+    q, sc = mgw.mxfp8_quantize_gather(hidden, torch.zeros(0, dtype=torch.int32, device="cuda"),
+                                      dev_i32([0, 0, 0]), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and not bool(q.any()) and not bool(sc.any())
