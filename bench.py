@@ -211,29 +211,71 @@ def run_wgrad(name, steps, warmup, dist_ctx):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
-    # end to end through the public API: pinned host inputs in, grad_w out to host
+    # End to end through the public API: every step copies its inputs from pinned host
+    # memory and its grad_w back to pinned host memory.  Steps are pipelined the way a
+    # training loop would run them: inputs and outputs are double-buffered on the device,
+    # and host-to-device copies, the kernels and device-to-host copies run on three streams
+    # ordered by events, so step i's grad_w download overlaps step i+1's upload and compute.
     out_host = torch.empty((E * N, K), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(3, min(steps, 20))
+    e2e_steps = max(4, min(steps, 20))
+    s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    bufs = []
+    for j in range(2):
+        bufs.append({
+            "g": g if j == 0 else torch.empty_like(g), "x": x if j == 0 else torch.empty_like(x),
+            "off": off if j == 0 else torch.empty_like(off),
+            "rows": (rows_dev if j == 0 else torch.empty_like(rows_dev)) if gather else None,
+            "out": out if j == 0 else torch.empty_like(out),
+            "in_free": torch.cuda.Event(), "in_ready": torch.cuda.Event(),
+            "out_ready": torch.cuda.Event(), "out_free": torch.cuda.Event()})
+    for bf in bufs:  # nothing in flight yet
+        bf["in_free"].record(s_comp)
+        bf["out_free"].record(s_d2h)
 
-    def e2e_step():
-        g.copy_(g_host, non_blocking=True)
-        x.copy_(x_host, non_blocking=True)
-        off.copy_(off_host, non_blocking=True)
-        if gather:
-            rows_dev.copy_(rows_host, non_blocking=True)
-        step()
-        out_host.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        bf = bufs[i % 2]
+        with torch.cuda.stream(s_h2d):
+            s_h2d.wait_event(bf["in_free"])
+            bf["g"].copy_(g_host, non_blocking=True)
+            bf["x"].copy_(x_host, non_blocking=True)
+            bf["off"].copy_(off_host, non_blocking=True)
+            if gather:
+                bf["rows"].copy_(rows_host, non_blocking=True)
+            bf["in_ready"].record(s_h2d)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(bf["in_ready"])
+            s_comp.wait_event(bf["out_free"])
+            mgw.mxfp8_quantize(bf["g"], bf["off"], Mcap, gq, gs, status, stream=s_comp)
+            if gather:
+                mgw.mxfp8_quantize_gather(bf["x"], bf["rows"], bf["off"], Mcap, xq, xs, status, stream=s_comp)
+            else:
+                mgw.mxfp8_quantize(bf["x"], bf["off"], Mcap, xq, xs, status, stream=s_comp)
+            mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, bf["off"], M, bf["out"], status, stream=s_comp)
+            bf["in_free"].record(s_comp)
+            bf["out_ready"].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(bf["out_ready"])
+            out_host.copy_(bf["out"], non_blocking=True)
+            bf["out_free"].record(s_d2h)
 
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     dist_ctx.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
+    a.record(s_h2d)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    # the timed region ends when the last step's grad_w has reached the host
+    s_h2d.wait_stream(s_d2h)
+    b.record(s_h2d)
     torch.cuda.synchronize()
     e2e_ms = dist_ctx.max(a.elapsed_time(b)) / e2e_steps
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the end-to-end leg")
+    # same inputs, deterministic kernels: the downloaded grad_w equals the device-timed one
+    if not torch.equal(out_host[:: max(1, out_host.shape[0] // 64)].to(dev), out[:: max(1, out.shape[0] // 64)]):
+        raise RuntimeError("end-to-end grad_w differs from the device-timed grad_w")
     h2d = g_host.numel() * 2 + x_host.numel() * 2 + off_host.numel() * 4 + (rows_host.numel() * 4 if gather else 0)
     d2h = out_host.numel() * 2
 

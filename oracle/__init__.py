@@ -79,6 +79,14 @@ def _load():
             lib.orc_grouped_dgrad.restype = None
             lib.orc_grouped_dgrad_element.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
             lib.orc_grouped_dgrad_element.restype = dbl
+            lib.orc_mxfp8_quantize_rows.argtypes = [P, i32, i32, P, i32, i64, i32, P, P]
+            lib.orc_mxfp8_quantize_rows.restype = None
+            lib.orc_mx_dot.argtypes = [P, P, P, P, i32]
+            lib.orc_mx_dot.restype = dbl
+            lib.orc_grouped_fprop_mx.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, P]
+            lib.orc_grouped_fprop_mx.restype = None
+            lib.orc_grouped_dgrad_mx.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i64, P]
+            lib.orc_grouped_dgrad_mx.restype = None
             _lib = lib
     return _lib
 
@@ -212,3 +220,60 @@ def grouped_dgrad_element(dy: np.ndarray, W: np.ndarray, expert_off, r: int, k: 
     v = _load().orc_grouped_dgrad_element(_ptr(dy), _ptr(W), _ptr(off), E, rows, out_f, in_f,
                                           r, k, ctypes.c_void_p(ctypes.addressof(b)))
     return v, b.value
+
+
+# ------------------------------------------- forward and data-gradient GEMMs (MXFP8)
+def mxfp8_quantize_rows(src_bf16_bits: np.ndarray, expert_off, Mcap: int | None = None,
+                        rule: int = SCALE_FLOOR):
+    """Row-wise MXFP8 quantization along the hidden axis (post-attn page: each token's
+    activations staged as MXFP8 with one e8m0 byte per 32 hidden features).  Rows of
+    expert e go to padded rows P[e] + (r - off[e]).
+
+    Returns (q [Mcap, C] uint8, sc [Mcap, C/32] uint8) in the plain layout."""
+    src = np.ascontiguousarray(src_bf16_bits, dtype=np.uint16)
+    M, C = src.shape
+    off = _off(expert_off)
+    E = off.size - 1
+    if Mcap is None:
+        Mcap = token_capacity(M, E)
+    q = np.empty((Mcap, C), dtype=np.uint8)
+    sc = np.empty((Mcap, C // 32), dtype=np.uint8)
+    _load().orc_mxfp8_quantize_rows(_ptr(src), M, C, _ptr(off), E, Mcap, int(rule), _ptr(q),
+                                    _ptr(sc))
+    return q, sc
+
+
+def mx_dot(aq, as_, bq, bs) -> float:
+    """sum_l deq(a)[l] deq(b)[l] of two MXFP8 vectors (one scale per 32 elements)."""
+    aq, as_, bq, bs = (np.ascontiguousarray(v, dtype=np.uint8) for v in (aq, as_, bq, bs))
+    L = aq.size
+    assert bq.size == L and as_.size == L // 32 and bs.size == L // 32
+    return float(_load().orc_mx_dot(_ptr(aq), _ptr(as_), _ptr(bq), _ptr(bs), L))
+
+
+def grouped_fprop_mx(xq, xs, wq, ws, expert_off, w_off, M: int) -> np.ndarray:
+    """fp64 y[r, n] = deq(x)[r] . deq(W)[e(r), n] over the hidden axis (post-attn page's
+    expert GEMMs, forward).  x row-wise quantized [Mcap, K]; W row-wise quantized stacked
+    [Mw, K] with expert e's rows from the padded start of ``w_off``."""
+    off, woff = _off(expert_off), _off(w_off)
+    E = off.size - 1
+    Mcap, K = xq.shape
+    N = int(woff[1] - woff[0])
+    out = np.empty((M, N), dtype=np.float64)
+    _load().orc_grouped_fprop_mx(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(off), _ptr(woff),
+                                 E, M, N, K, Mcap, _ptr(out))
+    return out
+
+
+def grouped_dgrad_mx(dyq, dys, wtq, wts, expert_off, w_off, M: int) -> np.ndarray:
+    """fp64 dx[r, k] = sum_n deq(dy)[r, n] deq(W)[e(r), n, k] (dgrad page, MXFP8 operands).
+    dy row-wise quantized [Mcap, N]; W quantized along n per expert (the token-axis
+    quantizer on W stacked [E*N, K] with ``w_off``): wtq [K, Mw]."""
+    off, woff = _off(expert_off), _off(w_off)
+    E = off.size - 1
+    Mcap, N = dyq.shape
+    K, Mw = wtq.shape
+    out = np.empty((M, K), dtype=np.float64)
+    _load().orc_grouped_dgrad_mx(_ptr(dyq), _ptr(dys), _ptr(wtq), _ptr(wts), _ptr(off),
+                                 _ptr(woff), E, M, N, K, Mcap, Mw, _ptr(out))
+    return out

@@ -251,3 +251,107 @@ void orc_grouped_dgrad(const float *dy, const float *W, const int32_t *off, int 
       if (bound) bound[(int64_t)r * in_f + k] = b;
     }
 }
+
+/* ------------------------------------------- forward and data-gradient GEMMs */
+
+/* The post-attn page stages every routed token's activations for its expert GEMMs as
+ * MXFP8 along the hidden axis: one e8m0 byte per 32 consecutive hidden features of a
+ * token (its XSC_WORDS = HIDDEN / 32 scale words per token row, and mx8_scale / mx8_q
+ * applied per 32-block).  Same rules as orc_mxfp8_quantize, blocks along a row. */
+void orc_mxfp8_quantize_rows(const uint16_t *src, int M, int C, const int32_t *off, int E,
+                             int64_t Mcap, int rule, uint8_t *q, uint8_t *sc) {
+  (void)M;
+  const int nb = C / 32;
+  memset(q, 0, (size_t)Mcap * (size_t)C);
+  memset(sc, 0, (size_t)Mcap * (size_t)nb);
+  int64_t *P = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E + 1));
+  orc_padded_starts(off, E, P);
+  for (int e = 0; e < E; ++e) {
+    const int cnt = off[e + 1] - off[e];
+    for (int i = 0; i < cnt; ++i) {
+      const uint16_t *row = src + (int64_t)(off[e] + i) * C;
+      const int64_t p = P[e] + i;
+      for (int j = 0; j < nb; ++j) {
+        double amax = 0.0;
+        for (int c = 32 * j; c < 32 * j + 32; ++c) {
+          const double v = fabs(orc_bf16_decode(row[c]));
+          if (v > amax) amax = v;
+        }
+        const uint8_t byte = rule ? orc_mx_scale_byte_ceil448(amax) : orc_mx_scale_byte(amax);
+        const int s = (int)byte - 127;
+        sc[p * nb + j] = byte;
+        for (int c = 32 * j; c < 32 * j + 32; ++c)
+          q[p * C + c] = orc_e4m3_encode_rne_satfinite(ldexp(orc_bf16_decode(row[c]), -s));
+      }
+    }
+  }
+  free(P);
+}
+
+/* Dot product of two MXFP8 vectors of L elements (L a multiple of 32), each with one
+ * e8m0 scale per 32 consecutive elements: sum_l deq(a)[l] * deq(b)[l] in fp64.  Every
+ * product is exact in fp64; only the sum rounds. */
+double orc_mx_dot(const uint8_t *aq, const uint8_t *as, const uint8_t *bq, const uint8_t *bs,
+                  int L) {
+  double acc = 0.0;
+  for (int l = 0; l < L; ++l)
+    acc += orc_e4m3_decode(aq[l]) * orc_e8m0_decode(as[l / 32]) *
+           (orc_e4m3_decode(bq[l]) * orc_e8m0_decode(bs[l / 32]));
+  return acc;
+}
+
+/* Expert of routed row r: the one whose row range [off[e], off[e+1]) holds it (the
+ * dgrad page's expert_for_row; empty experts hold no rows). */
+static int expert_of(const int32_t *off, int E, int r) {
+  return orc_expert_for_row_bsearch(off, E, r);
+}
+
+/* The post-attn page's expert GEMMs in the forward direction: each routed token's row
+ * times the transpose of its expert's weight matrix (W[e] stored [N, K], output features
+ * by hidden), both operands MXFP8 along the hidden axis K. */
+void orc_grouped_fprop_mx(const uint8_t *xq, const uint8_t *xs, const uint8_t *wq,
+                          const uint8_t *ws, const int32_t *off, const int32_t *w_off, int E,
+                          int M, int N, int K, int64_t Mcap, double *out) {
+  (void)Mcap;
+  const int nb = K / 32;
+  int64_t *P = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E + 1));
+  int64_t *Pw = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E + 1));
+  orc_padded_starts(off, E, P);
+  orc_padded_starts(w_off, E, Pw);
+  for (int r = 0; r < M; ++r) {
+    const int e = expert_of(off, E, r);
+    const int64_t p = P[e] + (r - off[e]);
+    for (int n = 0; n < N; ++n) {
+      const int64_t wr = Pw[e] + n; /* row of W[e][n] */
+      out[(int64_t)r * N + n] =
+          orc_mx_dot(xq + p * K, xs + p * nb, wq + wr * K, ws + wr * nb, K);
+    }
+  }
+  free(P);
+  free(Pw);
+}
+
+/* The dgrad page's dx[row, k] = sum_n dy[row, n] * W[e(row), n, k] with both operands in
+ * MXFP8 along n (the contraction axis): dy row-wise, W per expert along its n axis. */
+void orc_grouped_dgrad_mx(const uint8_t *dyq, const uint8_t *dys, const uint8_t *wtq,
+                          const uint8_t *wts, const int32_t *off, const int32_t *w_off, int E,
+                          int M, int N, int K, int64_t Mcap, int64_t Mw, double *out) {
+  (void)Mcap;
+  const int nb = N / 32;
+  int64_t *P = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E + 1));
+  int64_t *Pw = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E + 1));
+  orc_padded_starts(off, E, P);
+  orc_padded_starts(w_off, E, Pw);
+  for (int r = 0; r < M; ++r) {
+    const int e = expert_of(off, E, r);
+    const int64_t p = P[e] + (r - off[e]);
+    for (int k = 0; k < K; ++k) {
+      /* W[e][n][k] for n = 0.. is row k of wtq from column Pw[e] (a multiple of 128) */
+      const uint8_t *wrow = wtq + (int64_t)k * Mw + Pw[e];
+      const uint8_t *wsc = wts + (int64_t)k * (Mw / 32) + Pw[e] / 32;
+      out[(int64_t)r * K + k] = orc_mx_dot(dyq + p * N, dys + p * nb, wrow, wsc, N);
+    }
+  }
+  free(P);
+  free(Pw);
+}

@@ -76,6 +76,41 @@ void orc_grouped_dgrad(const float *dy, const float *W, const int32_t *off, int 
 double orc_grouped_dgrad_element(const float *dy, const float *W, const int32_t *off, int E,
                                  int rows, int out_f, int in_f, int r, int k, double *bound_out);
 
+/* ----------------------------------------------- forward and data-gradient GEMMs
+ * MXFP8 operands quantized along the hidden (contraction) axis of each row. */
+
+/* Row-wise MXFP8 quantization of a bf16 [M, C] row-major matrix: one scale per 32
+ * consecutive elements of a row (blocks along C, starting at column 0), rows of
+ * expert e placed at the padded rows P[e] + (r - off[e]).
+ *   q  : [Mcap, C] e4m3 bytes, row-major; padding rows 0.
+ *   sc : [Mcap, C/32] e8m0 bytes (plain layout); padding 0.
+ * rule as in orc_mxfp8_quantize. */
+void orc_mxfp8_quantize_rows(const uint16_t *src, int M, int C, const int32_t *off, int E,
+                             int64_t Mcap, int rule, uint8_t *q, uint8_t *sc);
+
+/* sum_l deq(a)[l] * deq(b)[l] over L elements (L % 32 == 0), one e8m0 scale per 32. */
+double orc_mx_dot(const uint8_t *aq, const uint8_t *as, const uint8_t *bq, const uint8_t *bs,
+                  int L);
+
+/* Grouped forward GEMM y[r, n] = sum_k deq(x)[r, k] * deq(W)[e(r), n, k] in fp64.
+ *   xq, xs : row-wise quantized x ([Mcap, K], plain scales [Mcap, K/32]), rows by off.
+ *   wq, ws : row-wise quantized W stacked [Mw, K] (plain scales [Mw, K/32]); W[e][n]
+ *            is row Pw[e] + n, Pw the padded starts of w_off (E+1 entries, e*N).
+ *   out    : [M, N]. */
+void orc_grouped_fprop_mx(const uint8_t *xq, const uint8_t *xs, const uint8_t *wq,
+                          const uint8_t *ws, const int32_t *off, const int32_t *w_off, int E,
+                          int M, int N, int K, int64_t Mcap, double *out);
+
+/* Grouped data gradient dx[r, k] = sum_n deq(dy)[r, n] * deq(W)[e(r), n, k] in fp64.
+ *   dyq, dys : row-wise quantized dy ([Mcap, N], plain scales [Mcap, N/32]), rows by off.
+ *   wtq, wts : W quantized along n per expert (orc_mxfp8_quantize of W stacked
+ *              [E*N, K] with w_off): [K, Mw] and plain scales [K, Mw/32]; W[e][n][k] is
+ *              column Pw[e] + n of row k.
+ *   out      : [M, K]. */
+void orc_grouped_dgrad_mx(const uint8_t *dyq, const uint8_t *dys, const uint8_t *wtq,
+                          const uint8_t *wts, const int32_t *off, const int32_t *w_off, int E,
+                          int M, int N, int K, int64_t Mcap, int64_t Mw, double *out);
+
 #ifdef __cplusplus
 }
 #endif
