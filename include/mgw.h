@@ -176,6 +176,70 @@ mgw_status mgw_grouped_dgrad_f32(const float *dy, const float *W, const int32_t 
                                  int E, int rows, int out_f, int in_f, float *dx,
                                  int *status_dev, void *stream);
 
+/* ---------------------------------------- forward and data gradient in MXFP8
+ * The expert GEMMs on routed rows with both operands MXFP8 along the contraction
+ * axis, as the post-attn page runs its expert GEMMs on MXFP8 activations and
+ * weights (one e8m0 byte per 32 hidden features of a token row; its wide MoE up
+ * and down stages).  Routed rows of expert e are expert_off[e] <= r <
+ * expert_off[e+1]; row-wise quantized operands hold them on a padded row axis of
+ * length Mcap, expert e's rows from P[e] (the padded starts above), so every
+ * 128-row tile belongs to one expert. */
+
+/* mgw_mxfp8_quantize_rows -- row-wise MXFP8 quantization (no transpose).
+ * For every routed row r of expert e and every block of 32 consecutive columns:
+ * the scale byte from the block's largest magnitude under scale_rule (as
+ * mgw_mxfp8_quantize), values scaled by the power of two and rounded to e4m3
+ * (nearest even, saturating to +-448), written to padded row P[e] + (r - off[e]).
+ *
+ * src_bf16    device, bf16 [src_rows, C] row-major (C contiguous).
+ * src_rows    rows of src when row_index is given; ignored otherwise.
+ * row_index   device int32 [M], nullable.  When given, routed row r reads row
+ *             row_index[r] of src (the unpermuted token matrix: the MoE gather);
+ *             an index outside [0, src_rows) gives a zero row and sets
+ *             MGW_DEV_BAD_INDEX.  When null, routed row r is row r of src [M, C].
+ * M           routed rows (>= 0); C a positive multiple of 128.
+ * expert_off  device int32 [E+1], 0 = off[0] <= ... <= off[E] = M.
+ * q_e4m3      device, [Mcap, C] row-major e4m3 bytes, fully written (padding rows 0).
+ * scales_e8m0 device, Mcap*C/32 bytes, fully written: 512-byte atoms, the atom of
+ *             128-column chunk c and 128-row tile t at byte (c*(Mcap/128) + t)*512,
+ *             row p%128 = r0 + 32*r1 and 32-column block kb of the chunk at
+ *             16*r0 + 4*r1 + kb (the layout mgw_mxfp8_quantize writes for a
+ *             [C, Mcap] operand, here for an [Mcap, C] one).  Padding bytes 0.
+ * Mcap        multiple of 128, >= mgw_mxfp8_token_capacity(M, E).
+ * All pointers 16-byte aligned.  Bad offsets: MGW_DEV_BAD_OFFSETS, outputs untouched. */
+mgw_status mgw_mxfp8_quantize_rows(const void *src_bf16, int src_rows, const int32_t *row_index,
+                                   int M, int C, const int32_t *expert_off, int E, void *q_e4m3,
+                                   void *scales_e8m0, size_t Mcap, int scale_rule,
+                                   int *status_dev, void *stream);
+
+/* mgw_grouped_fprop_mxfp8 -- grouped forward GEMM
+ *   y[r, n] = sum_k deq(x)[r, k] * deq(W)[e(r), n, k]
+ * xq, xs   x quantized by mgw_mxfp8_quantize_rows with expert_off: [Mcap, K].
+ * wq, ws   W [E, N, K] (bf16, nn.Linear layout) quantized by mgw_mxfp8_quantize_rows as
+ *          [E*N, K] with offsets {0, N, 2N, ..., E*N} (W[e][n] is row e*N + n):
+ *          [Mw, K] with Mw its Mcap.
+ * N a positive multiple of 256; K a positive multiple of 128.
+ * y_bf16   device, bf16 [M, N] row-major, fully written (round to nearest even).
+ * Accumulation is fp32 in tensor memory; no bound beyond fp32 summation error. */
+mgw_status mgw_grouped_fprop_mxfp8(const void *xq, const void *xs, const void *wq,
+                                   const void *ws, const int32_t *expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, size_t Mw, void *y_bf16,
+                                   int *status_dev, void *stream);
+
+/* mgw_grouped_dgrad_mxfp8 -- grouped data gradient with MXFP8 operands
+ *   dx[r, k] = sum_n deq(dy)[r, n] * deq(W)[e(r), n, k]
+ * (the dgrad page's product, contracted over the expert's output features n).
+ * dyq, dys dy [M, N] quantized by mgw_mxfp8_quantize_rows with expert_off: [Mcap, N].
+ * wtq, wts W [E, N, K] (bf16) quantized along n by mgw_mxfp8_quantize as [E*N, K]
+ *          tokens-by-features with offsets {0, N, ..., E*N}: [K, Mw] with Mw its Mcap,
+ *          W[e][n][k] at row k, column e*N + n.
+ * N a positive multiple of 128; K a positive multiple of 256.
+ * dx_bf16  device, bf16 [M, K] row-major, fully written. */
+mgw_status mgw_grouped_dgrad_mxfp8(const void *dyq, const void *dys, const void *wtq,
+                                   const void *wts, const int32_t *expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, size_t Mw, void *dx_bf16,
+                                   int *status_dev, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

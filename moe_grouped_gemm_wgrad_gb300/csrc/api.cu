@@ -244,3 +244,107 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
 }
 
 }  // extern "C"
+
+namespace {
+
+mgw_status grouped_mm_impl(const void* aq, const void* as, const void* bq, const void* bs,
+                           const int32_t* expert_off, int E, int M, int J, int L, size_t Mcap,
+                           uint64_t RB, uint64_t LB, long long b_row_step, long long b_col_step,
+                           void* out_bf16, int* status_dev, void* stream) {
+  DeviceInfo dev;
+  mgw_status st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  mgw::MmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  // With M == 0 there is no routed row and the output map is never used.
+  const void* out_base = M > 0 ? out_bf16 : aq;
+  const uint64_t out_rows = M > 0 ? static_cast<uint64_t>(M) : 1;
+  if (!make_map_2d(&a.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, L, Mcap, L, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, LB, RB, LB, 128, 256,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_base, J, out_rows,
+                   static_cast<uint64_t>(J) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MGW_ERR_CUDA;
+  a.out = out_bf16;
+  a.as = static_cast<const uint8_t*>(as);
+  a.bs = static_cast<const uint8_t*>(bs);
+  a.expert_off = expert_off;
+  a.E = E;
+  a.M = M;
+  a.J = J;
+  a.L = L;
+  a.Mcap = static_cast<long long>(Mcap);
+  a.RB = static_cast<long long>(RB);
+  a.b_row_step = b_row_step;
+  a.b_col_step = b_col_step;
+  a.status = status_dev;
+  const cudaError_t err = mgw::launch_grouped_mm_mxfp8(a, dev.sms, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mgw_status mgw_mxfp8_quantize_rows(const void* src_bf16, int src_rows, const int32_t* row_index,
+                                   int M, int C, const int32_t* expert_off, int E, void* q_e4m3,
+                                   void* scales_e8m0, size_t Mcap, int scale_rule,
+                                   int* status_dev, void* stream) {
+  if (!expert_off || !q_e4m3 || !scales_e8m0 || (M > 0 && !src_bf16)) return MGW_ERR_INVALID_ARG;
+  if (M < 0 || C <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
+  if (scale_rule != MGW_SCALE_FLOOR && scale_rule != MGW_SCALE_CEIL_448) return MGW_ERR_INVALID_ARG;
+  if (row_index != nullptr && M > 0 && src_rows < 1) return MGW_ERR_INVALID_ARG;
+  if (C % 128 != 0) return MGW_ERR_UNSUPPORTED;
+  if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if ((src_bf16 && !aligned16(src_bf16)) || !aligned16(q_e4m3) || !aligned16(scales_e8m0))
+    return MGW_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  mgw_status st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  const cudaError_t err = mgw::launch_mxfp8_quantize_rows(
+      src_bf16, row_index != nullptr ? src_rows : M, row_index, M, C, expert_off, E, q_e4m3,
+      scales_e8m0, static_cast<long long>(Mcap), scale_rule, status_dev, dev.sms,
+      static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+mgw_status mgw_grouped_fprop_mxfp8(const void* xq, const void* xs, const void* wq,
+                                   const void* ws, const int32_t* expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, size_t Mw, void* y_bf16,
+                                   int* status_dev, void* stream) {
+  if (!xq || !xs || !wq || !ws || !expert_off || (M > 0 && !y_bf16)) return MGW_ERR_INVALID_ARG;
+  if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
+  if (N % 256 != 0 || K % 128 != 0) return MGW_ERR_UNSUPPORTED;
+  if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if (Mw % 128 != 0 || Mw < static_cast<size_t>(E) * N || Mw > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if (!aligned16(xq) || !aligned16(xs) || !aligned16(wq) || !aligned16(ws) ||
+      (y_bf16 && !aligned16(y_bf16)))
+    return MGW_ERR_INVALID_ARG;
+  return grouped_mm_impl(xq, xs, wq, ws, expert_off, E, M, N, K, Mcap, Mw, K, N, 0, y_bf16,
+                         status_dev, stream);
+}
+
+mgw_status mgw_grouped_dgrad_mxfp8(const void* dyq, const void* dys, const void* wtq,
+                                   const void* wts, const int32_t* expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, size_t Mw, void* dx_bf16,
+                                   int* status_dev, void* stream) {
+  if (!dyq || !dys || !wtq || !wts || !expert_off || (M > 0 && !dx_bf16))
+    return MGW_ERR_INVALID_ARG;
+  if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 256 != 0) return MGW_ERR_UNSUPPORTED;
+  if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if (Mw % 128 != 0 || Mw < static_cast<size_t>(E) * N || Mw > (size_t(1) << 31))
+    return MGW_ERR_CAPACITY;
+  if (!aligned16(dyq) || !aligned16(dys) || !aligned16(wtq) || !aligned16(wts) ||
+      (dx_bf16 && !aligned16(dx_bf16)))
+    return MGW_ERR_INVALID_ARG;
+  return grouped_mm_impl(dyq, dys, wtq, wts, expert_off, E, M, K, N, Mcap, K, Mw, 0, N, dx_bf16,
+                         status_dev, stream);
+}
+
+}  // extern "C"

@@ -44,6 +44,32 @@ struct WgradArgs {
 };
 cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream);
 
+// Row-wise MXFP8 quantization (quantize_rows.cu): routed row r (source row row_index[r],
+// or r when row_index is null) of expert e goes to padded row P[e] + r - off[e] of
+// q [Mcap, C]; scale atoms per (128-column chunk, 128-row tile).
+size_t quantize_rows_smem_bytes(int E);
+cudaError_t launch_mxfp8_quantize_rows(const void* src, int src_rows, const int32_t* row_index,
+                                       int M, int C, const int32_t* expert_off, int E, void* q,
+                                       void* sc, long long Mcap, int rule, int* status,
+                                       int num_sms, cudaStream_t stream);
+
+// M-grouped MXFP8 GEMM (grouped_mm.cu): out[r, j] = sum_l A[p(r), l] * B[e*b_row_step + j,
+// e*b_col_step + l], r a routed row of expert e, p(r) its padded row.
+struct MmArgs {
+  CUtensorMap tm_a;    // A e4m3 [Mcap, L], box 128 x 128 rows, 128B swizzle
+  CUtensorMap tm_b;    // B e4m3 [RB, LB], box 128 x 256 rows, 128B swizzle
+  CUtensorMap tm_out;  // out bf16 [M, J], box 64 cols x 128 rows, 128B swizzle
+  void* out;           // out (plain stores of tiles that end inside an expert's last rows)
+  const uint8_t* as;   // A scale atoms, (chunk * Mcap/128 + row tile) * 512
+  const uint8_t* bs;   // B scale atoms, (chunk * RB/128 + row tile) * 512
+  const int32_t* expert_off;
+  int E, M, J, L;
+  long long Mcap, RB;
+  long long b_row_step, b_col_step;
+  int* status;
+};
+cudaError_t launch_grouped_mm_mxfp8(const MmArgs& a, int num_sms, cudaStream_t stream);
+
 struct DgradArgs {
   const float* dy;
   const float* W;

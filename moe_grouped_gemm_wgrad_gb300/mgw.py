@@ -27,7 +27,8 @@ SCALE_CEIL_448 = 1   # the post-attn page's RoundUp rule ceil_pow2(amax / 448)
 EXPORTS = (
     "mgw_status_string", "mgw_version", "mgw_mxfp8_token_capacity", "mgw_mxfp8_scale_bytes",
     "mgw_mxfp8_quantize", "mgw_mxfp8_quantize_gather", "mgw_grouped_wgrad_mxfp8",
-    "mgw_grouped_dgrad_f32",
+    "mgw_grouped_dgrad_f32", "mgw_mxfp8_quantize_rows", "mgw_grouped_fprop_mxfp8",
+    "mgw_grouped_dgrad_mxfp8",
 )
 
 
@@ -65,6 +66,12 @@ def load() -> ctypes.CDLL:
         lib.mgw_grouped_wgrad_mxfp8.restype = I
         lib.mgw_grouped_dgrad_f32.argtypes = [P, P, P, I, I, I, I, P, P, P]
         lib.mgw_grouped_dgrad_f32.restype = I
+        lib.mgw_mxfp8_quantize_rows.argtypes = [P, I, P, I, I, P, I, P, P, SZ, I, P, P]
+        lib.mgw_mxfp8_quantize_rows.restype = I
+        lib.mgw_grouped_fprop_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
+        lib.mgw_grouped_fprop_mxfp8.restype = I
+        lib.mgw_grouped_dgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
+        lib.mgw_grouped_dgrad_mxfp8.restype = I
         _lib = lib
         return lib
 
@@ -180,4 +187,74 @@ def grouped_dgrad_f32(dy: torch.Tensor, W: torch.Tensor, expert_off: torch.Tenso
     st = load().mgw_grouped_dgrad_f32(_ptr(dy), _ptr(W), _ptr(expert_off), E, rows, out_f, in_f,
                                       _ptr(out), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_dgrad_f32")
+    return out
+
+
+def mxfp8_quantize_rows(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int | None = None,
+                        q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                        status: torch.Tensor | None = None, stream=None,
+                        scale_rule: int = SCALE_FLOOR, row_index: torch.Tensor | None = None):
+    """Row-wise MXFP8 quantization (one scale per 32 columns of a row) of the routed rows:
+    ``src[row_index]`` when ``row_index`` (int32 [M]) is given, else ``src`` [M, C].
+    -> (q uint8 [Mcap, C] on the padded row axis, scale atoms uint8)."""
+    _dev_tensor(src, torch.bfloat16, "src")
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    src_rows, C = src.shape
+    if row_index is not None:
+        _dev_tensor(row_index, torch.int32, "row_index")
+        M = row_index.numel()
+    else:
+        M = src_rows
+    E = expert_off.numel() - 1
+    if Mcap is None:
+        Mcap = token_capacity(M, E)
+    if q is None:
+        q = torch.empty((Mcap, C), dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
+    st = load().mgw_mxfp8_quantize_rows(_ptr(src), src_rows, _ptr(row_index), M, C,
+                                        _ptr(expert_off), E, _ptr(q), _ptr(scales), Mcap,
+                                        int(scale_rule), _ptr(status), _stream(stream))
+    _check(st, "mgw_mxfp8_quantize_rows")
+    return q, scales
+
+
+def grouped_fprop_mxfp8(xq: torch.Tensor, xs: torch.Tensor, wq: torch.Tensor, ws: torch.Tensor,
+                        expert_off: torch.Tensor, M: int, N: int, out: torch.Tensor | None = None,
+                        status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y [M, N] bf16 = x[r] . W[e(r)]^T from row-wise quantized x [Mcap, K] and W [Mw, K]
+    (W [E, N, K] quantized with offsets {0, N, ..., E*N})."""
+    for t, n in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
+        _dev_tensor(t, torch.uint8, n)
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    Mcap, K = xq.shape
+    Mw = wq.shape[0]
+    E = expert_off.numel() - 1
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    st = load().mgw_grouped_fprop_mxfp8(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(expert_off),
+                                        E, int(M), int(N), K, Mcap, Mw, _ptr(out), _ptr(status),
+                                        _stream(stream))
+    _check(st, "mgw_grouped_fprop_mxfp8")
+    return out
+
+
+def grouped_dgrad_mxfp8(dyq: torch.Tensor, dys: torch.Tensor, wtq: torch.Tensor,
+                        wts: torch.Tensor, expert_off: torch.Tensor, M: int,
+                        out: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """dx [M, K] bf16 = dy[r] . W[e(r)] from row-wise quantized dy [Mcap, N] and W quantized
+    along n per expert by :func:`mxfp8_quantize` (wtq [K, Mw])."""
+    for t, n in ((dyq, "dyq"), (dys, "dys"), (wtq, "wtq"), (wts, "wts")):
+        _dev_tensor(t, torch.uint8, n)
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    Mcap, N = dyq.shape
+    K, Mw = wtq.shape
+    E = expert_off.numel() - 1
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=dyq.device)
+    st = load().mgw_grouped_dgrad_mxfp8(_ptr(dyq), _ptr(dys), _ptr(wtq), _ptr(wts),
+                                        _ptr(expert_off), E, int(M), N, K, Mcap, Mw, _ptr(out),
+                                        _ptr(status), _stream(stream))
+    _check(st, "mgw_grouped_dgrad_mxfp8")
     return out

@@ -71,3 +71,28 @@ def test_argument_errors_before_device_work(lib):
     assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1, 4, 32, 128, fake, None, None) == -2
     assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1, 4, 48, 256, fake, None, None) == -2
     assert lib.mgw_grouped_dgrad_f32(fake, None, fake, 1, 4, 32, 256, fake, None, None) == -1
+
+
+def test_argument_errors_forward_and_mx_dgrad(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # row-wise quantize: null offsets, C not a multiple of 128, small Mcap, bad rule,
+    # row index without a source row count, misaligned output
+    assert lib.mgw_mxfp8_quantize_rows(fake, 4, None, 4, 128, None, 1, fake, fake, 256, 0, None, None) == -1
+    assert lib.mgw_mxfp8_quantize_rows(fake, 4, None, 4, 96, fake, 1, fake, fake, 256, 0, None, None) == -2
+    assert lib.mgw_mxfp8_quantize_rows(fake, 300, None, 300, 128, fake, 2, fake, fake, 384, 0, None, None) == -3
+    assert lib.mgw_mxfp8_quantize_rows(fake, 4, None, 4, 128, fake, 1, fake, fake, 256, 2, None, None) == -1
+    assert lib.mgw_mxfp8_quantize_rows(fake, 0, fake, 4, 128, fake, 1, fake, fake, 256, 0, None, None) == -1
+    assert lib.mgw_mxfp8_quantize_rows(fake, 4, None, 4, 128, fake, 1, P(0x1008), fake, 256, 0, None, None) == -1
+    # forward: N not a multiple of 256, K not a multiple of 128, Mw too small, Mcap too small
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 1, 4, 256, 64, 256, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 2, 4, 256, 128, 384, 384, fake, None, None) == -3
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 2, 300, 256, 128, 384, 512, fake, None, None) == -3
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, None, fake, fake, 1, 4, 256, 128, 256, 256, fake, None, None) == -1
+    # MXFP8 data gradient: N not a multiple of 128, K not a multiple of 256, misaligned
+    assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 64, 256, 256, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, 256, fake, None, None) == -2
+    assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, P(0x1004), fake, fake, 1, 4, 128, 256, 256, 256, fake, None, None) == -1
+    # no rows: the output may be null only then
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 1, 4, 256, 128, 256, 256, None, None, None) == -1
