@@ -327,6 +327,74 @@ def run_dgrad(name, steps, warmup):
             "l2": "flushed between launches (256 MB write)"}
 
 
+def run_mx_pair(name, steps, warmup):
+    """The MXFP8 forward and data-gradient GEMMs of the MoE FFN pair: per step the routed
+    rows are gathered and quantized along hidden, W is quantized both ways, then
+    y = x W[e]^T and dx = dy W[e].  Per-kernel CUDA events; every operand is larger
+    than L2 or read once per step."""
+    import torch
+
+    from moe_grouped_gemm_wgrad_gb300 import mgw
+
+    from moe_grouped_gemm_wgrad_gb300 import synth
+
+    if name == "moe_ffn_small":  # 2048 tokens x top-8 of 16 experts: a small profiling case
+        wg, dg = synth.moe_ffn_pair(tokens=2048, E=16)
+    else:
+        wg, dg = wgrad_case(name), dgrad_case(name)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, N, K, M = wg.E, wg.N, wg.K, wg.M
+    w_off_h = np.arange(E + 1, dtype=np.int32) * N
+    hidden = torch.from_numpy(wg.meta["hidden_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    tok = torch.from_numpy(wg.meta["token_of_row"]).to(dev)
+    dy = torch.from_numpy(wg.g_bf16.view(np.int16)).to(dev).view(torch.bfloat16)
+    W = torch.from_numpy(synth.bf16_bits_from_f32(dg.W.reshape(E * N, K)).view(np.int16)).to(dev).view(torch.bfloat16)
+    off = torch.from_numpy(wg.expert_off).to(dev)
+    w_off = torch.from_numpy(w_off_h).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    Mcap = mgw.token_capacity(M, E)
+    xq, xs = mgw.mxfp8_quantize_rows(hidden, off, Mcap, row_index=tok, status=status)
+    wq, ws = mgw.mxfp8_quantize_rows(W, w_off, status=status)
+    dyq, dys = mgw.mxfp8_quantize_rows(dy, off, Mcap, status=status)
+    wtq, wts = mgw.mxfp8_quantize(W, w_off, status=status)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def kernels():
+        return [
+            lambda: mgw.mxfp8_quantize_rows(hidden, off, Mcap, xq, xs, status, row_index=tok),
+            lambda: mgw.mxfp8_quantize_rows(W, w_off, wq.shape[0], wq, ws, status),
+            lambda: mgw.grouped_fprop_mxfp8(xq, xs, wq, ws, off, M, N, y, status),
+            lambda: mgw.mxfp8_quantize_rows(dy, off, Mcap, dyq, dys, status),
+            lambda: mgw.mxfp8_quantize(W, w_off, wtq.shape[1], wtq, wts, status),
+            lambda: mgw.grouped_dgrad_mxfp8(dyq, dys, wtq, wts, off, M, dx, status),
+        ]
+
+    ks = kernels()
+    for _ in range(warmup):
+        for k in ks:
+            k()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ks) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, k in enumerate(ks):
+            k()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(ks))]
+    flops = 2.0 * M * N * K
+    names = ["quantize_rows_x_gather", "quantize_rows_w", "grouped_fprop_mxfp8", "quantize_rows_dy",
+             "quantize_w_along_n", "grouped_dgrad_mxfp8"]
+    return {"workload": name, "rows": M, "ffn": N, "hidden": K, "experts": E,
+            "kernels_ms": dict(zip(names, ms)),
+            "fprop_tflops": flops / (ms[2] * 1e-3) / 1e12, "dgrad_mx_tflops": flops / (ms[5] * 1e-3) / 1e12,
+            "launches_per_step": len(ks)}
+
+
 # ------------------------------------------------------------ CPU baseline
 def oracle_wgrad_sample(case, n_sub: int, k_sub: int):
     """Times the oracle (as it stands, single thread) on expert 0's tokens for an
@@ -407,6 +475,7 @@ def main():
     ap.add_argument("--workload", default="wgrad_8192",
                     choices=["wgrad_tiny", "wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
     ap.add_argument("--dgrad-workload", default="dgrad_4096", choices=["dgrad_4096", "moe_ffn_pair", "none"])
+    ap.add_argument("--mx-workload", default="moe_ffn_pair", choices=["moe_ffn_pair", "moe_ffn_small", "none"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     peaks = _peaks()
@@ -456,6 +525,9 @@ def main():
     dg = None
     if args.dgrad_workload != "none":
         dg = run_dgrad(args.dgrad_workload, max(5, min(args.steps, 50)), max(3, args.warmup))
+    mx = None
+    if args.mx_workload != "none":
+        mx = run_mx_pair(args.mx_workload, max(5, min(args.steps, 20)), max(3, args.warmup))
     case = r["case"]
     value = r["flops"] * d.world / (r["ms_per_step"] * 1e-3) / 1e12
     wg_tflops = r["flops"] / (r["wgrad_ms"] * 1e-3) / 1e12
@@ -501,6 +573,10 @@ def main():
                               "unit": "TFLOP/s", "frac": 3 * dg["tflops"] / tf32_peak,
                               "note": "3xTF32: three tf32 MMAs per fp32 product"}
             line["dgrad"] = dg
+        if mx is not None:
+            for key in ("fprop_tflops", "dgrad_mx_tflops"):
+                mx[key.replace("tflops", "frac_of_burst")] = mx[key] / mxfp8_burst
+            line["mx_forward_dgrad"] = mx
         print(json.dumps(line))
     d.close()
 
