@@ -155,6 +155,40 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void *gq, const void *gs, const void *x
                                    int N, int K, size_t Mcap, void *out_bf16, int *status_dev,
                                    void *stream);
 
+/* -------------------------------------------------- wgrad under skewed routing
+ * mgw_grouped_wgrad_mxfp8_balanced -- the same result as mgw_grouped_wgrad_mxfp8 (same
+ * operands, layout, output and tolerance), computed with split-K over tokens and dynamic
+ * scheduling for routings where a few experts hold most tokens.
+ *
+ * The wgrad page runs one block per (expert, output tile) over all of that expert's tokens
+ * (its expert decode from the block index); with one huge expert a few blocks then carry
+ * most of the work.  Here an expert whose 128-token chunks exceed a target item length L
+ * (about all chunks / (2 x SM count), at least 8) is split into S = ceil(chunks / L) <= 16
+ * token ranges per output tile; each range's fp32 partial goes to the workspace and the
+ * range that finishes last sums the S partials in range order (so results are
+ * deterministic) and stores bf16.  Items are handed out longest first by an atomic counter
+ * in the workspace.  L is doubled until the partials fit the workspace; a workspace of
+ * only the 256-byte header gives dynamic scheduling without splits.
+ *
+ * Arguments as mgw_grouped_wgrad_mxfp8, plus:
+ * workspace        device, 256-byte aligned, workspace_bytes long, zero-filled before its
+ *                  first use.  Every call that ends without MGW_DEV_TIMEOUT returns its
+ *                  counters (the first 256 + 4 x slots bytes) to zero, so it is reused as
+ *                  is; after a time-out it must be zero-filled again.  Calls sharing a
+ *                  workspace must not run concurrently.
+ * workspace_bytes  >= 256 (else MGW_ERR_CAPACITY); mgw_grouped_wgrad_workspace_bytes gives
+ *                  a size with room for 2 x SM count partial tiles (128 KB each).
+ * E <= 512 (else MGW_ERR_UNSUPPORTED). */
+mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void *gq, const void *gs, const void *xq,
+                                            const void *xs, const int32_t *expert_off, int E,
+                                            int M, int N, int K, size_t Mcap, void *out_bf16,
+                                            void *workspace, size_t workspace_bytes,
+                                            int *status_dev, void *stream);
+
+/* Workspace size for mgw_grouped_wgrad_mxfp8_balanced on the current device: 2 x SM count
+ * partial tiles plus counters (about 38 MB on a 152-SM GB300).  0 if no usable device. */
+size_t mgw_grouped_wgrad_workspace_bytes(int E, int N, int K);
+
 /* ---------------------------------------------------------------- dgrad
  * mgw_grouped_dgrad_f32 -- grouped data gradient
  *   dx[r, k] = sum_n dy[r, n] * W[e(r), n, k]

@@ -169,10 +169,13 @@ mgw_status mgw_mxfp8_quantize_gather(const void* src_bf16, int src_rows,
                        q_e4m3, scales_e8m0, Mcap, scale_rule, status_dev, stream);
 }
 
-mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* xq,
-                                   const void* xs, const int32_t* expert_off, int E, int M,
-                                   int N, int K, size_t Mcap, void* out_bf16, int* status_dev,
-                                   void* stream) {
+}  // extern "C"
+
+namespace {
+
+mgw_status wgrad_check(const void* gq, const void* gs, const void* xq, const void* xs,
+                       const int32_t* expert_off, int E, int M, int N, int K, size_t Mcap,
+                       void* out_bf16) {
   if (!gq || !gs || !xq || !xs || !expert_off || !out_bf16) return MGW_ERR_INVALID_ARG;
   if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 256 != 0) return MGW_ERR_UNSUPPORTED;
@@ -181,34 +184,89 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* x
     return MGW_ERR_CAPACITY;
   if (!aligned16(gq) || !aligned16(xq) || !aligned16(gs) || !aligned16(xs) || !aligned16(out_bf16))
     return MGW_ERR_INVALID_ARG;
+  return MGW_OK;
+}
+
+// Tensor maps and sizes of the wgrad kernels; box_b is the x^T box height (256, or 128 for
+// CTA pairs).
+bool wgrad_maps(mgw::WgradArgs* a, const void* gq, const void* gs, const void* xq,
+                const void* xs, const int32_t* expert_off, int E, int M, int N, int K,
+                size_t Mcap, void* out_bf16, int* status_dev, uint32_t box_b) {
+  std::memset(a, 0, sizeof(*a));
+  if (!make_map_2d(&a->tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, Mcap, N, Mcap, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a->tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128, box_b,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a->tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, 256,
+                   static_cast<uint64_t>(N) * (Mcap / 32) / 256, 256, 256, 2,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&a->tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, 256,
+                   static_cast<uint64_t>(K) * (Mcap / 32) / 256, 256, 256, 4,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&a->tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_bf16, K,
+                   static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return false;
+  a->out = out_bf16;
+  a->gs = static_cast<const uint8_t*>(gs);
+  a->xs = static_cast<const uint8_t*>(xs);
+  a->expert_off = expert_off;
+  a->E = E;
+  a->M = M;
+  a->N = N;
+  a->K = K;
+  a->status = status_dev;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mgw_grouped_wgrad_workspace_bytes(int E, int N, int K) {
+  (void)E;
+  (void)N;
+  (void)K;
+  DeviceInfo dev;
+  if (current_device(&dev) != MGW_OK) return 0;
+  return mgw::balanced_workspace_bytes(2 * dev.sms);
+}
+
+mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void* gq, const void* gs, const void* xq,
+                                            const void* xs, const int32_t* expert_off, int E,
+                                            int M, int N, int K, size_t Mcap, void* out_bf16,
+                                            void* workspace, size_t workspace_bytes,
+                                            int* status_dev, void* stream) {
+  mgw_status st = wgrad_check(gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16);
+  if (st != MGW_OK) return st;
+  if (E > mgw::kMaxBalancedExperts) return MGW_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MGW_ERR_INVALID_ARG;
+  const int slots = mgw::balanced_workspace_slots(workspace_bytes);
+  if (slots < 0) return MGW_ERR_CAPACITY;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  mgw::WgradArgs a;
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev, 256))
+    return MGW_ERR_CUDA;
+  const cudaError_t err = mgw::launch_grouped_wgrad_balanced(a, workspace, slots, dev.sms,
+                                                             static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
+mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* xq,
+                                   const void* xs, const int32_t* expert_off, int E, int M,
+                                   int N, int K, size_t Mcap, void* out_bf16, int* status_dev,
+                                   void* stream) {
+  mgw_status st0 = wgrad_check(gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16);
+  if (st0 != MGW_OK) return st0;
   DeviceInfo dev;
   mgw_status st = current_device(&dev);
   if (st != MGW_OK) return st;
   mgw::WgradArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!make_map_2d(&a.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, Mcap, N, Mcap, 128, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128,
-                   mgw::wgrad_uses_pair(N) ? 128 : 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&a.tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, 256,
-                   static_cast<uint64_t>(N) * (Mcap / 32) / 256, 256, 256, 2,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&a.tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, 256,
-                   static_cast<uint64_t>(K) * (Mcap / 32) / 256, 256, 256, 4,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&a.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_bf16, K,
-                   static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev,
+                  mgw::wgrad_uses_pair(N) ? 128 : 256))
     return MGW_ERR_CUDA;
-  a.out = out_bf16;
-  a.gs = static_cast<const uint8_t*>(gs);
-  a.xs = static_cast<const uint8_t*>(xs);
-  a.expert_off = expert_off;
-  a.E = E;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.status = status_dev;
   {
     const char* v = std::getenv("MGW_TEST_DROP_LOAD");  // test hook, see kernels.h
     a.drop_first_load = (v != nullptr && v[0] == '1') ? 1 : 0;

@@ -41,8 +41,24 @@ struct WgradArgs {
   // announces its first chunk's bytes but never issues the copies, so the waits on that
   // stage run out and the kernel reports MGW_DEV_TIMEOUT.  Zero in normal use.
   int drop_first_load;
+  // Load-balanced kernel only (wgrad_balanced.cu): the workspace.
+  int* ws_sched;   // [0] next item, [1] CTAs finished (zero at rest)
+  int* ws_cnt;     // per split tile: parts finished (zero at rest), ws_slots entries
+  float* ws_part;  // ws_slots fp32 128 x 256 partial tiles
+  int ws_slots;
 };
 cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream);
+
+// Load-balanced wgrad (wgrad_balanced.cu).  Workspace: a 256-byte header (item and CTA
+// counters), ws_slots int tile counters (padded to 256 bytes), then ws_slots 128 KB fp32
+// partial tiles.  Zero-filled before the first call; every call that ends without a
+// device time-out leaves it zero-filled again.
+constexpr int kMaxBalancedExperts = 512;
+constexpr size_t kWsHeaderBytes = 256;
+int balanced_workspace_slots(size_t bytes);   // -1 when smaller than the header
+size_t balanced_workspace_bytes(int slots);
+cudaError_t launch_grouped_wgrad_balanced(WgradArgs a, void* workspace, int slots, int num_sms,
+                                          cudaStream_t stream);
 
 // Row-wise MXFP8 quantization (quantize_rows.cu): routed row r (source row row_index[r],
 // or r when row_index is null) of expert e goes to padded row P[e] + r - off[e] of

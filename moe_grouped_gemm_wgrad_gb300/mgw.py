@@ -28,7 +28,8 @@ EXPORTS = (
     "mgw_status_string", "mgw_version", "mgw_mxfp8_token_capacity", "mgw_mxfp8_scale_bytes",
     "mgw_mxfp8_quantize", "mgw_mxfp8_quantize_gather", "mgw_grouped_wgrad_mxfp8",
     "mgw_grouped_dgrad_f32", "mgw_mxfp8_quantize_rows", "mgw_grouped_fprop_mxfp8",
-    "mgw_grouped_dgrad_mxfp8",
+    "mgw_grouped_dgrad_mxfp8", "mgw_grouped_wgrad_mxfp8_balanced",
+    "mgw_grouped_wgrad_workspace_bytes",
 )
 
 
@@ -72,6 +73,10 @@ def load() -> ctypes.CDLL:
         lib.mgw_grouped_fprop_mxfp8.restype = I
         lib.mgw_grouped_dgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
         lib.mgw_grouped_dgrad_mxfp8.restype = I
+        lib.mgw_grouped_wgrad_mxfp8_balanced.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, SZ, P, P]
+        lib.mgw_grouped_wgrad_mxfp8_balanced.restype = I
+        lib.mgw_grouped_wgrad_workspace_bytes.argtypes = [I, I, I]
+        lib.mgw_grouped_wgrad_workspace_bytes.restype = SZ
         _lib = lib
         return lib
 
@@ -170,6 +175,38 @@ def grouped_wgrad_mxfp8(gq: torch.Tensor, gs: torch.Tensor, xq: torch.Tensor, xs
                                         E, int(M), N, K, Mcap, _ptr(out), _ptr(status),
                                         _stream(stream))
     _check(st, "mgw_grouped_wgrad_mxfp8")
+    return out
+
+
+def wgrad_workspace(E: int, N: int, K: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for :func:`grouped_wgrad_mxfp8_balanced` on ``device``."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        nbytes = int(load().mgw_grouped_wgrad_workspace_bytes(int(E), int(N), int(K)))
+    if nbytes == 0:
+        raise MgwError("mgw_grouped_wgrad_workspace_bytes: no usable device")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+
+
+def grouped_wgrad_mxfp8_balanced(gq: torch.Tensor, gs: torch.Tensor, xq: torch.Tensor,
+                                 xs: torch.Tensor, expert_off: torch.Tensor, M: int,
+                                 workspace: torch.Tensor, out: torch.Tensor | None = None,
+                                 status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """grad_w [E*N, K] bf16, as :func:`grouped_wgrad_mxfp8`, with split-K and dynamic
+    scheduling for skewed routings.  ``workspace``: uint8, zero-filled before first use
+    (see :func:`wgrad_workspace`); calls sharing it must not overlap."""
+    for t, n in ((gq, "gq"), (gs, "gs"), (xq, "xq"), (xs, "xs"), (workspace, "workspace")):
+        _dev_tensor(t, torch.uint8, n)
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    N, Mcap = gq.shape
+    K = xq.shape[0]
+    E = expert_off.numel() - 1
+    if out is None:
+        out = torch.empty((E * N, K), dtype=torch.bfloat16, device=gq.device)
+    st = load().mgw_grouped_wgrad_mxfp8_balanced(
+        _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
+        _ptr(out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check(st, "mgw_grouped_wgrad_mxfp8_balanced")
     return out
 
 

@@ -96,3 +96,21 @@ def test_argument_errors_forward_and_mx_dgrad(lib):
     assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, P(0x1004), fake, fake, 1, 4, 128, 256, 256, 256, fake, None, None) == -1
     # no rows: the output may be null only then
     assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 1, 4, 256, 128, 256, 256, None, None, None) == -1
+
+
+def test_argument_errors_balanced_wgrad(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    ws = P(0x10000)  # 256-byte aligned
+    args = [fake, fake, fake, fake, fake, 1, 4, 128, 256, 256, fake]
+    # missing or misaligned workspace
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced(*args, None, 1 << 20, None, None) == -1
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced(*args, P(0x10010), 1 << 20, None, None) == -1
+    # workspace smaller than its 256-byte header
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced(*args, ws, 255, None, None) == -3
+    # more experts than the balanced kernel's tables hold
+    big = [fake, fake, fake, fake, fake, 513, 4, 128, 256, 1 << 17, fake]
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced(*big, ws, 1 << 20, None, None) == -2
+    # the static kernel's checks apply too
+    bad_k = [fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, fake]
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced(*bad_k, ws, 1 << 20, None, None) == -2
