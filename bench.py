@@ -395,6 +395,59 @@ def run_mx_pair(name, steps, warmup):
             "launches_per_step": len(ks)}
 
 
+def run_wgrad_kernels(name, steps, warmup):
+    """The static and the load-balanced wgrad kernels on one workload, launches alternated,
+    each timed with CUDA events (output larger than L2)."""
+    import torch
+
+    from moe_grouped_gemm_wgrad_gb300 import mgw
+
+    case = wgrad_case(name)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    off = torch.from_numpy(case.expert_off).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    Mcap = mgw.token_capacity(case.M, case.E)
+    g = torch.from_numpy(case.g_bf16.view(np.int16)).to(dev).view(torch.bfloat16)
+    if "hidden_bf16" in case.meta:
+        hidden = torch.from_numpy(case.meta["hidden_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+        rows = torch.from_numpy(case.meta["token_of_row"]).to(dev)
+        xq, xs = mgw.mxfp8_quantize_gather(hidden, rows, off, Mcap, status=status)
+    else:
+        x = torch.from_numpy(case.x_bf16.view(np.int16)).to(dev).view(torch.bfloat16)
+        xq, xs = mgw.mxfp8_quantize(x, off, Mcap, status=status)
+    gq, gs = mgw.mxfp8_quantize(g, off, Mcap, status=status)
+    out = torch.empty((case.E * case.N, case.K), dtype=torch.bfloat16, device=dev)
+    ws = mgw.wgrad_workspace(case.E, case.N, case.K)
+    stream = torch.cuda.current_stream()
+    kern = {
+        "static": lambda: mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, case.M, out, status),
+        "balanced": lambda: mgw.grouped_wgrad_mxfp8_balanced(gq, gs, xq, xs, off, case.M, ws, out, status),
+    }
+    for _ in range(warmup):
+        for k in kern.values():
+            k()
+    torch.cuda.synchronize()
+    ev = {n: [] for n in kern}
+    for _ in range(steps):
+        for n, k in kern.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            k()
+            b.record(stream)
+            ev[n].append((a, b))
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    flops = 2.0 * case.M * case.N * case.K
+    nbytes = (case.N + case.K) * Mcap * (1 + 1 / 32) + case.E * case.N * case.K * 2
+    res = {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "experts": case.E}
+    for n in kern:
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev[n])
+        res[n] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "hbm_gbs": nbytes / (ms * 1e-3) / 1e9}
+    res["algorithmic_bytes"] = nbytes
+    return res
+
+
 # ------------------------------------------------------------ CPU baseline
 def oracle_wgrad_sample(case, n_sub: int, k_sub: int):
     """Times the oracle (as it stands, single thread) on expert 0's tokens for an
@@ -476,6 +529,8 @@ def main():
                     choices=["wgrad_tiny", "wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
     ap.add_argument("--dgrad-workload", default="dgrad_4096", choices=["dgrad_4096", "moe_ffn_pair", "none"])
     ap.add_argument("--mx-workload", default="moe_ffn_pair", choices=["moe_ffn_pair", "moe_ffn_small", "none"])
+    ap.add_argument("--skew-workload", default="wgrad_skew",
+                    choices=["wgrad_skew", "wgrad_8192", "moe_ffn_pair", "none"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     peaks = _peaks()
@@ -525,6 +580,9 @@ def main():
     dg = None
     if args.dgrad_workload != "none":
         dg = run_dgrad(args.dgrad_workload, max(5, min(args.steps, 50)), max(3, args.warmup))
+    sk = None
+    if args.skew_workload != "none":
+        sk = run_wgrad_kernels(args.skew_workload, max(5, min(args.steps, 50)), max(3, args.warmup))
     mx = None
     if args.mx_workload != "none":
         mx = run_mx_pair(args.mx_workload, max(5, min(args.steps, 20)), max(3, args.warmup))
@@ -573,6 +631,8 @@ def main():
                               "unit": "TFLOP/s", "frac": 3 * dg["tflops"] / tf32_peak,
                               "note": "3xTF32: three tf32 MMAs per fp32 product"}
             line["dgrad"] = dg
+        if sk is not None:
+            line["wgrad_static_vs_balanced"] = sk
         if mx is not None:
             for key in ("fprop_tflops", "dgrad_mx_tflops"):
                 mx[key.replace("tflops", "frac_of_burst")] = mx[key] / mxfp8_burst
