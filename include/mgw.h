@@ -185,6 +185,19 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void *gq, const void *gs, cons
                                             void *workspace, size_t workspace_bytes,
                                             int *status_dev, void *stream);
 
+/* mgw_grouped_wgrad_mxfp8_balanced_noalloc -- mgw_grouped_wgrad_mxfp8_balanced on a
+ * workspace the library owns: a 16 MB device array (room for 128 partial tiles) defined in
+ * the library and zero-filled when it loads, one per device.  The call allocates no memory
+ * and takes no workspace argument.  Because every call on a device shares that array,
+ * calls on different streams must not run concurrently; after MGW_DEV_TIMEOUT the array's
+ * counters are undefined and the process must not use this entry point again.  Arguments,
+ * result and errors otherwise as mgw_grouped_wgrad_mxfp8_balanced. */
+mgw_status mgw_grouped_wgrad_mxfp8_balanced_noalloc(const void *gq, const void *gs,
+                                                    const void *xq, const void *xs,
+                                                    const int32_t *expert_off, int E, int M,
+                                                    int N, int K, size_t Mcap, void *out_bf16,
+                                                    int *status_dev, void *stream);
+
 /* Workspace size for mgw_grouped_wgrad_mxfp8_balanced on the current device: 2 x SM count
  * partial tiles plus counters (about 38 MB on a 152-SM GB300).  0 if no usable device. */
 size_t mgw_grouped_wgrad_workspace_bytes(int E, int N, int K);

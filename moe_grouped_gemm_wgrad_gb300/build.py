@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmgw.so")
-SOURCES = ["api.cu", "quantize.cu", "quantize_rows.cu", "wgrad.cu", "wgrad_balanced.cu", "grouped_mm.cu", "dgrad.cu"]
+SOURCES = ["api.cu", "quantize.cu", "quantize_rows.cu", "wgrad.cu", "wgrad_balanced.cu", "wgrad_noalloc.cu", "grouped_mm.cu", "dgrad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v"]

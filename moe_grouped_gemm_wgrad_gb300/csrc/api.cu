@@ -254,6 +254,29 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void* gq, const void* gs, cons
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }
 
+mgw_status mgw_grouped_wgrad_mxfp8_balanced_noalloc(const void* gq, const void* gs,
+                                                    const void* xq, const void* xs,
+                                                    const int32_t* expert_off, int E, int M,
+                                                    int N, int K, size_t Mcap, void* out_bf16,
+                                                    int* status_dev, void* stream) {
+  mgw_status st = wgrad_check(gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16);
+  if (st != MGW_OK) return st;
+  if (E > mgw::kMaxBalancedExperts) return MGW_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != MGW_OK) return st;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (mgw::noalloc_wgrad_workspace(&ws, &ws_bytes) != cudaSuccess) return MGW_ERR_CUDA;
+  const int slots = mgw::balanced_workspace_slots(ws_bytes);
+  mgw::WgradArgs a;
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev, 256))
+    return MGW_ERR_CUDA;
+  const cudaError_t err = mgw::launch_grouped_wgrad_balanced(a, ws, slots, dev.sms,
+                                                             static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
+}
+
 mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* xq,
                                    const void* xs, const int32_t* expert_off, int E, int M,
                                    int N, int K, size_t Mcap, void* out_bf16, int* status_dev,

@@ -59,6 +59,8 @@ int balanced_workspace_slots(size_t bytes);   // -1 when smaller than the header
 size_t balanced_workspace_bytes(int slots);
 cudaError_t launch_grouped_wgrad_balanced(WgradArgs a, void* workspace, int slots, int num_sms,
                                           cudaStream_t stream);
+// The library-owned workspace of the no-allocation entry point (wgrad_noalloc.cu).
+cudaError_t noalloc_wgrad_workspace(void** ptr, size_t* bytes);
 
 // Row-wise MXFP8 quantization (quantize_rows.cu): routed row r (source row row_index[r],
 // or r when row_index is null) of expert e goes to padded row P[e] + r - off[e] of

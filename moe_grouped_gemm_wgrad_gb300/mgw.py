@@ -29,7 +29,7 @@ EXPORTS = (
     "mgw_mxfp8_quantize", "mgw_mxfp8_quantize_gather", "mgw_grouped_wgrad_mxfp8",
     "mgw_grouped_dgrad_f32", "mgw_mxfp8_quantize_rows", "mgw_grouped_fprop_mxfp8",
     "mgw_grouped_dgrad_mxfp8", "mgw_grouped_wgrad_mxfp8_balanced",
-    "mgw_grouped_wgrad_workspace_bytes",
+    "mgw_grouped_wgrad_workspace_bytes", "mgw_grouped_wgrad_mxfp8_balanced_noalloc",
 )
 
 
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.mgw_grouped_wgrad_mxfp8_balanced.restype = I
         lib.mgw_grouped_wgrad_workspace_bytes.argtypes = [I, I, I]
         lib.mgw_grouped_wgrad_workspace_bytes.restype = SZ
+        lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
+        lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -207,6 +209,28 @@ def grouped_wgrad_mxfp8_balanced(gq: torch.Tensor, gs: torch.Tensor, xq: torch.T
         _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
         _ptr(out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_wgrad_mxfp8_balanced")
+    return out
+
+
+def grouped_wgrad_mxfp8_balanced_noalloc(gq: torch.Tensor, gs: torch.Tensor, xq: torch.Tensor,
+                                         xs: torch.Tensor, expert_off: torch.Tensor, M: int,
+                                         out: torch.Tensor | None = None,
+                                         status: torch.Tensor | None = None,
+                                         stream=None) -> torch.Tensor:
+    """As :func:`grouped_wgrad_mxfp8_balanced` on the library's own workspace (a device array
+    in the library; nothing is allocated, calls must not overlap)."""
+    for t, n in ((gq, "gq"), (gs, "gs"), (xq, "xq"), (xs, "xs")):
+        _dev_tensor(t, torch.uint8, n)
+    _dev_tensor(expert_off, torch.int32, "expert_off")
+    N, Mcap = gq.shape
+    K = xq.shape[0]
+    E = expert_off.numel() - 1
+    if out is None:
+        out = torch.empty((E * N, K), dtype=torch.bfloat16, device=gq.device)
+    st = load().mgw_grouped_wgrad_mxfp8_balanced_noalloc(
+        _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
+        _ptr(out), _ptr(status), _stream(stream))
+    _check(st, "mgw_grouped_wgrad_mxfp8_balanced_noalloc")
     return out
 
 

@@ -114,3 +114,12 @@ def test_argument_errors_balanced_wgrad(lib):
     # the static kernel's checks apply too
     bad_k = [fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, fake]
     assert lib.mgw_grouped_wgrad_mxfp8_balanced(*bad_k, ws, 1 << 20, None, None) == -2
+
+
+def test_argument_errors_noalloc_wgrad(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc(
+        None, fake, fake, fake, fake, 1, 4, 128, 256, 256, fake, None, None) == -1
+    assert lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc(
+        fake, fake, fake, fake, fake, 513, 4, 128, 256, 1 << 17, fake, None, None) == -2
