@@ -217,7 +217,7 @@ def run_wgrad(name, steps, warmup, dist_ctx):
     # and host-to-device copies, the kernels and device-to-host copies run on three streams
     # ordered by events, so step i's grad_w download overlaps step i+1's upload and compute.
     out_host = torch.empty((E * N, K), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(4, min(steps, 20))
+    e2e_steps = max(4, min(steps, 40))
     s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     bufs = []
     for j in range(2):
