@@ -17,8 +17,8 @@
 //   part finished last, writes bf16 and resets the counter.  No CTA waits for another.
 // * Dynamic scheduling.  Items (expert, tile, part) are ordered by descending part length
 //   and handed out by an atomic counter in the workspace, one item ahead, so every CTA takes
-//   the next longest item when it is free (greedy LPT).  The producer publishes each item
-//   through a two-slot shared-memory ring to the MMA thread and the epilogue.  The last CTA
+//   the next longest item when it is free (greedy LPT).  The producer decodes each item and
+//   publishes it through a two-slot shared-memory ring to the MMA thread and the epilogue.  The last CTA
 //   to finish resets the counter, leaving the workspace zero-filled for the next call.
 //
 // Tiles of experts without tokens are written with zeros by a dedicated warp (static
@@ -49,7 +49,8 @@ constexpr int kOffBar = kOffSf + kStages * kSfStage;
 // full[], empty[], acc_full, acc_empty, done, item_full[], item_empty[]
 constexpr int kNumBars = 2 * kStages + 3 + 2 * kItemSlots;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffTable = kOffMisc + 32;
+constexpr int kOffRing = kOffMisc + 16;
+constexpr int kOffTable = kOffRing + kItemSlots * 8 * 4;
 constexpr int kThreads = 352;
 constexpr int kEpiWarps = 8;
 constexpr int kZeroWarp = 10;
@@ -135,8 +136,19 @@ __device__ __forceinline__ Item decode_item(int it, int E, int tiles, int tiles_
   x.nt = x.tile / tiles_k;
   x.kt = x.tile % tiles_k;
   const int ch = (s_off[x.e + 1] - s_off[x.e] + BT - 1) / BT;
-  x.c0 = static_cast<int>(static_cast<long long>(x.part) * ch / x.S);
-  x.c1 = static_cast<int>(static_cast<long long>(x.part + 1) * ch / x.S);
+  x.c0 = x.part * ch / x.S;  // part <= 16 and ch < 2^24: no overflow
+  x.c1 = (x.part + 1) * ch / x.S;
+  return x;
+}
+
+__device__ __forceinline__ void ring_put(volatile int* slot, const Item& x) {
+  slot[0] = x.e, slot[1] = x.nt, slot[2] = x.kt, slot[3] = x.tile;
+  slot[4] = x.part, slot[5] = x.S, slot[6] = x.c0, slot[7] = x.c1;
+}
+__device__ __forceinline__ Item ring_get(const volatile int* slot) {
+  Item x;
+  x.e = slot[0], x.nt = slot[1], x.kt = slot[2], x.tile = slot[3];
+  x.part = slot[4], x.S = slot[5], x.c0 = slot[6], x.c1 = slot[7];
   return x;
 }
 
@@ -145,9 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int E = args.E, N = args.N, K = args.K;
-  // misc: [0] tmem base [1] abort [2] flag [3] last-part flag [4..5] item ring
+  // misc: [0] tmem base [1] abort [2] flag [3] last-part flag; then the item ring: per slot
+  // the decoded item (e, nt, kt, tile, part, S, c0, c1), e = -1 after the last item
   int* s_misc = reinterpret_cast<int*>(smem + kOffMisc);
-  volatile int* s_items = reinterpret_cast<volatile int*>(&s_misc[4]);
+  volatile int* s_ring = reinterpret_cast<volatile int*>(smem + kOffRing);
   int* s_off = reinterpret_cast<int*>(smem + kOffTable);
   int* s_pad = s_off + (E + 1);
   int* s_ipref = s_pad + (E + 1);
@@ -281,11 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
           ok = false;
           break;
         }
-        s_items[islot] = have ? it : -1;
+        Item x{-1, 0, 0, 0, 0, 1, 0, 0};
+        if (have) x = decode_item(it, E, tiles, tiles_k, s_off, s_ipref, s_order, s_split);
+        ring_put(s_ring + 8 * islot, x);
         mbar_arrive(bar_item_full(islot));
         if (++islot == kItemSlots) islot = 0, iph ^= 1u;
         if (!have) break;
-        const Item x = decode_item(it, E, tiles, tiles_k, s_off, s_ipref, s_order, s_split);
         const int ch0 = s_pad[x.e] / BT;
         for (int c = x.c0; c < x.c1; ++c) {
           if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
@@ -337,11 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
           ok = false;
           break;
         }
-        const int it = s_items[islot];
+        const Item x = ring_get(s_ring + 8 * islot);
         mbar_arrive(bar_item_empty(islot));
         if (++islot == kItemSlots) islot = 0, iph ^= 1u;
-        if (it < 0) break;
-        const Item x = decode_item(it, E, tiles, tiles_k, s_off, s_ipref, s_order, s_split);
+        if (x.e < 0) break;
         const int cnt = s_off[x.e + 1] - s_off[x.e];
         if (!stage_scales(stage, phase) || !mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -414,12 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
         if (lane == 0 && args.status) atomicOr(args.status, kDevTimeout);
         break;
       }
-      const int it = s_items[islot];
+      const Item x = ring_get(s_ring + 8 * islot);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_item_empty(islot));
       if (++islot == kItemSlots) islot = 0, iph ^= 1u;
-      if (it < 0) break;
-      const Item x = decode_item(it, E, tiles, tiles_k, s_off, s_ipref, s_order, s_split);
+      if (x.e < 0) break;
       uint32_t r[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) r[j] = 0u;
