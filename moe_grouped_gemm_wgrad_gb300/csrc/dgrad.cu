@@ -22,7 +22,8 @@
 //               accumulators (2 x 256 columns), so the epilogue of one item
 //               overlaps the main loop of the next.
 //   warps 5-12  transform: load dy and W tiles from global memory one chunk ahead
-//               (software pipelined in registers), split into hi/lo, write K-major
+//               (software pipelined in registers; the chunk after that is prefetched
+//               into L2), split into hi/lo, write K-major
 //               128B-swizzled tiles (W transposed on the fly) into a 2-stage
 //               shared-memory ring.
 #include <cstdint>
@@ -49,6 +50,8 @@ constexpr int kMmaWarp = 4;
 constexpr int kXfWarps = 8;
 constexpr int kThreads = (kEpiWarps + 1 + kXfWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
+// Chunks between the one loaded into registers and the one prefetched into L2.
+constexpr int kPrefetchAhead = 1;
 
 __host__ __device__ constexpr size_t dgrad_smem_bytes(int E) {
   return static_cast<size_t>(kOffTable) + sizeof(int) * (3 * static_cast<size_t>(E) + 3) + 1024;
@@ -191,6 +194,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
         for (int q = 0; q < 4; ++q) raw.b[p][q] = __ldg(src + static_cast<size_t>(q) * in_f);
       }
     };
+    // L2 prefetch of a chunk: its 32 W row segments (8 lines each) and 128 dy row segments
+    // (one line each), 384 lines over 256 threads, so that the register loads one chunk
+    // later hit L2 instead of waiting on DRAM.
+    auto prefetch_chunk = [&](const Item& item, int c) {
+      const int row0 = s_off[item.e] + item.rt * BM;
+      const int valid = min(BM, s_off[item.e + 1] - row0);
+      const float* Wk = args.W + static_cast<size_t>(item.e) * out_f * in_f + item.kt * BN;
+      for (int i = xt; i < 384; i += 256) {
+        const float* p;
+        if (i < 256) {
+          p = Wk + static_cast<size_t>(c * BK + (i >> 3)) * in_f + (i & 7) * 32;
+        } else {
+          const int r = i - 256;
+          if (r >= valid) continue;
+          p = args.dy + static_cast<size_t>(row0 + r) * out_f + c * BK;
+        }
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      }
+    };
+    // (item, c) -> the chunk after it in this CTA's sequence; false past the last
+    auto advance = [&](long long& it2, Item& item2, int& c2) -> bool {
+      if (++c2 == nchunks) {
+        c2 = 0;
+        it2 += gridDim.x;
+        if (it2 >= total) return false;
+        item2 = decode_item(it2, tiles_k, s_rtp, E);
+      }
+      return true;
+    };
     long long it = blockIdx.x;
     Raw cur, nxt;
     Item item{0, 0, 0};
@@ -209,7 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
         nit = it + gridDim.x;
         if (nit < total) nitem = decode_item(nit, tiles_k, s_rtp, E);
       }
-      if (nit < total) load_chunk(nitem, nc, nxt);
+      if (nit < total) {
+        load_chunk(nitem, nc, nxt);
+        long long pit = nit;
+        Item pitem = nitem;
+        int pc = nc;
+        bool more = true;
+        for (int d = 0; d < kPrefetchAhead && more; ++d) more = advance(pit, pitem, pc);
+        if (more) prefetch_chunk(pitem, pc);
+      }
       if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
         ok = false;
         break;
