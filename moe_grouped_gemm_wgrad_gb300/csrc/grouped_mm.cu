@@ -235,12 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mm_mxfp8_kernel(const __g
         for (int c = 0; c < nch; ++c) {
           const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
           const uint32_t sa = sbase + stage * kStageBytes;
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            mma_mxf8_block32(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
-                             sdesc_kmajor_sw128(sa + kABytes + 32 * kb),
-                             idesc_mxf8_e4m3(BM, BN, kb, kb), tsf, tsf + 8, (c | kb) != 0);
-          }
+          mma_mxf8_chunk128<BM, BN>(tmem, sdesc_kmajor_sw128(sa), sdesc_kmajor_sw128(sa + kABytes),
+                                    tsf, tsf + 8, c != 0);
           const int cur = stage;
           if (++stage == kStages) stage = 0, phase ^= 1u;
           if (c + 1 < nch && !stage_scales(stage, phase)) {

@@ -302,4 +302,17 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The four block-scaled MMAs (K = 32 each) of one 128-element K chunk of K-major,
+// 128B-swizzled A and B tiles: the 32-byte K step is +2 in the descriptors' start-address
+// field, and the instruction descriptors (scale-factor byte ids 0..3) are constants, so the
+// issuing thread spends as few instructions as possible between MMAs.
+template <int M, int N>
+__device__ __forceinline__ void mma_mxf8_chunk128(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                                  uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  mma_mxf8_block32(d, adesc, bdesc, idesc_mxf8_e4m3(M, N, 0, 0), sfa, sfb, accumulate);
+  mma_mxf8_block32(d, adesc + 2, bdesc + 2, idesc_mxf8_e4m3(M, N, 1, 1), sfa, sfb, 1u);
+  mma_mxf8_block32(d, adesc + 4, bdesc + 4, idesc_mxf8_e4m3(M, N, 2, 2), sfa, sfb, 1u);
+  mma_mxf8_block32(d, adesc + 6, bdesc + 6, idesc_mxf8_e4m3(M, N, 3, 3), sfa, sfb, 1u);
+}
+
 }  // namespace mgw

@@ -251,10 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
           const int rem = cnt - c * BT;
           const int nkb = rem >= BT ? 4 : (rem + 31) / 32;
           const uint32_t sa = sbase + stage * kStageBytes;
-          for (int kb = 0; kb < nkb; ++kb) {
-            mma_mxf8_block32(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
-                             sdesc_kmajor_sw128(sa + kABytes + 32 * kb),
-                             idesc_mxf8_e4m3(BM, BN, kb, kb), tsf, tsf + 8, (c | kb) != 0);
+          if (nkb == 4) {
+            mma_mxf8_chunk128<BM, BN>(tmem, sdesc_kmajor_sw128(sa), sdesc_kmajor_sw128(sa + kABytes),
+                                      tsf, tsf + 8, c != 0);
+          } else {
+            for (int kb = 0; kb < nkb; ++kb) {
+              mma_mxf8_block32(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
+                               sdesc_kmajor_sw128(sa + kABytes + 32 * kb),
+                               idesc_mxf8_e4m3(BM, BN, kb, kb), tsf, tsf + 8, (c | kb) != 0);
+            }
           }
           const int cur = stage;
           if (++stage == kStages) stage = 0, phase ^= 1u;
