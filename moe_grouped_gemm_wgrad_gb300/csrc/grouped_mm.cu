@@ -216,14 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mm_mxfp8_kernel(const __g
       bool ok = true;
       // Waits for the chunk in `st` and copies its scale atoms to the stage's TMEM slot,
       // one chunk ahead of that chunk's MMAs.
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
+      const uint64_t sf_desc0 = make_sdesc(sbase + kOffSf, 0, 128, 0);
       auto stage_scales = [&](int st, uint32_t ph) -> bool {
         if (!mbar_wait(bar_full(st), ph, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ssf = sbase + kOffSf + st * kSfStage;
+        const uint64_t d = sf_desc0 + static_cast<uint32_t>(st * (kSfStage >> 4));
         const uint32_t tsf = tmem + kSfCol0 + 16u * st;
-        tmem_cp_32x128b_warpx4(tsf, make_sdesc(ssf, 0, 128, 0));
-        tmem_cp_32x128b_warpx4(tsf + 8, make_sdesc(ssf + 512, 0, 128, 0));
-        tmem_cp_32x128b_warpx4(tsf + 12, make_sdesc(ssf + 1024, 0, 128, 0));
+        tmem_cp_32x128b_warpx4(tsf, d);
+        tmem_cp_32x128b_warpx4(tsf + 8, d + (512 >> 4));
+        tmem_cp_32x128b_warpx4(tsf + 12, d + (1024 >> 4));
         return true;
       };
       for (long long it = first; it < total && ok; it += step) {
@@ -234,9 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mm_mxfp8_kernel(const __g
         tc_fence_after();
         for (int c = 0; c < nch; ++c) {
           const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
-          const uint32_t sa = sbase + stage * kStageBytes;
-          mma_mxf8_chunk128<BM, BN>(tmem, sdesc_kmajor_sw128(sa), sdesc_kmajor_sw128(sa + kABytes),
-                                    tsf, tsf + 8, c != 0);
+          const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
+          mma_mxf8_chunk128<BM, BN>(tmem, ad, ad + (kABytes >> 4), tsf, tsf + 8, c != 0);
           const int cur = stage;
           if (++stage == kStages) stage = 0, phase ^= 1u;
           if (c + 1 < nch && !stage_scales(stage, phase)) {

@@ -223,14 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       // Waits for the chunk in `stage` to land and copies its scale atoms to the stage's
       // TMEM slot (32 rows x 16 B each, 8-row core matrices 128 B apart).  Issued one
       // chunk ahead of that chunk's MMAs so the copy overlaps the previous chunk's MMAs.
+      // Descriptors of stage 0; stage s adds its byte offset / 16 to the start-address field
+      // (the whole ring lies below 256 KB, so the 14-bit field never carries).
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
+      const uint64_t sf_desc0 = make_sdesc(sbase + kOffSf, 0, 128, 0);
       auto stage_scales = [&](int st, uint32_t ph) -> bool {
         if (!mbar_wait_spin(bar_full(st), ph, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ssf = sbase + kOffSf + st * kSfStage;
+        const uint64_t d = sf_desc0 + static_cast<uint32_t>(st * (kSfStage >> 4));
         const uint32_t tsf = tmem + kSfCol0 + 16u * st;
-        tmem_cp_32x128b_warpx4(tsf, make_sdesc(ssf, 0, 128, 0));
-        tmem_cp_32x128b_warpx4(tsf + 8, make_sdesc(ssf + 512, 0, 128, 0));
-        tmem_cp_32x128b_warpx4(tsf + 12, make_sdesc(ssf + 1024, 0, 128, 0));
+        tmem_cp_32x128b_warpx4(tsf, d);
+        tmem_cp_32x128b_warpx4(tsf + 8, d + (512 >> 4));
+        tmem_cp_32x128b_warpx4(tsf + 12, d + (1024 >> 4));
         return true;
       };
       ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
@@ -240,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
         const int cnt = s_off[e + 1] - s_off[e];
         if (cnt == 0) continue;
         const int nch = (cnt + BT - 1) / BT;
+        const int full_chunks = cnt / BT;  // chunks whose four 32-token blocks all hold tokens
         // first chunk's scales go in while the epilogue still drains the accumulator
         if (!stage_scales(stage, phase) || !mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -248,17 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
         tc_fence_after();
         for (int c = 0; c < nch; ++c) {
           const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
-          const int rem = cnt - c * BT;
-          const int nkb = rem >= BT ? 4 : (rem + 31) / 32;
-          const uint32_t sa = sbase + stage * kStageBytes;
-          if (nkb == 4) {
-            mma_mxf8_chunk128<BM, BN>(tmem, sdesc_kmajor_sw128(sa), sdesc_kmajor_sw128(sa + kABytes),
-                                      tsf, tsf + 8, c != 0);
+          const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
+          const uint64_t bd = ad + (kABytes >> 4);
+          if (c < full_chunks) {
+            mma_mxf8_chunk128<BM, BN>(tmem, ad, bd, tsf, tsf + 8, c != 0);
           } else {
+            const int nkb = (cnt - c * BT + 31) / 32;
             for (int kb = 0; kb < nkb; ++kb) {
-              mma_mxf8_block32(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
-                               sdesc_kmajor_sw128(sa + kABytes + 32 * kb),
-                               idesc_mxf8_e4m3(BM, BN, kb, kb), tsf, tsf + 8, (c | kb) != 0);
+              mma_mxf8_block32(tmem, ad + 2 * kb, bd + 2 * kb, idesc_mxf8_e4m3(BM, BN, kb, kb),
+                               tsf, tsf + 8, (c | kb) != 0);
             }
           }
           const int cur = stage;

@@ -336,14 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
       bool ok = true;
       int islot = 0;
       uint32_t iph = 0;
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
+      const uint64_t sf_desc0 = make_sdesc(sbase + kOffSf, 0, 128, 0);
       auto stage_scales = [&](int st, uint32_t ph) -> bool {
         if (!mbar_wait(bar_full(st), ph, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ssf = sbase + kOffSf + st * kSfStage;
+        const uint64_t d = sf_desc0 + static_cast<uint32_t>(st * (kSfStage >> 4));
         const uint32_t tsf = tmem + kSfCol0 + 16u * st;
-        tmem_cp_32x128b_warpx4(tsf, make_sdesc(ssf, 0, 128, 0));
-        tmem_cp_32x128b_warpx4(tsf + 8, make_sdesc(ssf + 512, 0, 128, 0));
-        tmem_cp_32x128b_warpx4(tsf + 12, make_sdesc(ssf + 1024, 0, 128, 0));
+        tmem_cp_32x128b_warpx4(tsf, d);
+        tmem_cp_32x128b_warpx4(tsf + 8, d + (512 >> 4));
+        tmem_cp_32x128b_warpx4(tsf + 12, d + (1024 >> 4));
         return true;
       };
       while (ok) {
@@ -361,20 +363,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
           break;
         }
         tc_fence_after();
+        const int full_chunks = cnt / BT;
         for (int c = x.c0; c < x.c1; ++c) {
           const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
-          const int rem = cnt - c * BT;
-          const int nkb = rem >= BT ? 4 : (rem + 31) / 32;
-          const uint32_t sa = sbase + stage * kStageBytes;
-          if (nkb == 4) {
-            mma_mxf8_chunk128<BM, BN>(tmem, sdesc_kmajor_sw128(sa), sdesc_kmajor_sw128(sa + kABytes),
-                                      tsf, tsf + 8, c != x.c0 ? 1u : 0u);
+          const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
+          const uint64_t bd = ad + (kABytes >> 4);
+          if (c < full_chunks) {
+            mma_mxf8_chunk128<BM, BN>(tmem, ad, bd, tsf, tsf + 8, c != x.c0 ? 1u : 0u);
           } else {
+            const int nkb = (cnt - c * BT + 31) / 32;
             for (int kb = 0; kb < nkb; ++kb) {
-              mma_mxf8_block32(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
-                               sdesc_kmajor_sw128(sa + kABytes + 32 * kb),
-                               idesc_mxf8_e4m3(BM, BN, kb, kb), tsf, tsf + 8,
-                               (c != x.c0 || kb != 0) ? 1u : 0u);
+              mma_mxf8_block32(tmem, ad + 2 * kb, bd + 2 * kb, idesc_mxf8_e4m3(BM, BN, kb, kb),
+                               tsf, tsf + 8, (c != x.c0 || kb != 0) ? 1u : 0u);
             }
           }
           const int cur = stage;
