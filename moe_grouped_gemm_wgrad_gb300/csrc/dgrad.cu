@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       int local = 0;
       bool ok = true;
       constexpr uint32_t idesc = idesc_tf32(BM, BN);
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
       for (long long it = blockIdx.x; it < total && ok; it += gridDim.x, ++local) {
         const int b = local & 1;
         if (!mbar_wait_spin(bar_acc_empty(b), acc_phase[b] ^ 1u, abort_flag)) {
@@ -315,18 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
             break;
           }
           tc_fence_after();
-          const uint32_t s_ahi = sbase + stage * kStageBytes;
-          const uint32_t s_alo = s_ahi + kATile;
-          const uint32_t s_bhi = s_alo + kATile;
-          const uint32_t s_blo = s_bhi + kBTile;
+          // descriptors from one base: tiles and the 32-byte K steps are offsets / 16 in the
+          // start-address field (the ring lies below 256 KB: no carry)
+          const uint64_t ahi = a_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
+          const uint64_t alo = ahi + (kATile >> 4);
+          const uint64_t bhi = alo + (kATile >> 4);
+          const uint64_t blo = bhi + (kBTile >> 4);
 #pragma unroll
           for (int ks = 0; ks < BK / 8; ++ks) {
-            const uint32_t ko = 32u * ks;  // 8 tf32 = 32 bytes along K
-            const uint64_t ahi = sdesc_kmajor_sw128(s_ahi + ko), alo = sdesc_kmajor_sw128(s_alo + ko);
-            const uint64_t bhi = sdesc_kmajor_sw128(s_bhi + ko), blo = sdesc_kmajor_sw128(s_blo + ko);
-            mma_tf32(dacc, alo, bhi, idesc, (c | ks) != 0);
-            mma_tf32(dacc, ahi, blo, idesc, 1u);
-            mma_tf32(dacc, ahi, bhi, idesc, 1u);
+            mma_tf32(dacc, alo + 2 * ks, bhi + 2 * ks, idesc, (c | ks) != 0);
+            mma_tf32(dacc, ahi + 2 * ks, blo + 2 * ks, idesc, 1u);
+            mma_tf32(dacc, ahi + 2 * ks, bhi + 2 * ks, idesc, 1u);
           }
           mma_commit(bar_empty(stage));
           if (++stage == kStages) stage = 0, phase ^= 1u;
