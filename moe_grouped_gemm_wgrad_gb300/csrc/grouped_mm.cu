@@ -238,13 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mm_mxfp8_kernel(const __g
           const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
           const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
           mma_mxf8_chunk128<BM, BN>(tmem, ad, ad + (kABytes >> 4), tsf, tsf + 8, c != 0);
-          const int cur = stage;
+          // release the stage as soon as its MMAs are issued, then prepare the next one
+          mma_commit(bar_empty(stage));
           if (++stage == kStages) stage = 0, phase ^= 1u;
           if (c + 1 < nch && !stage_scales(stage, phase)) {
             ok = false;
             break;
           }
-          mma_commit(bar_empty(cur));
         }
         if (!ok) break;
         mma_commit(bar_acc_full);

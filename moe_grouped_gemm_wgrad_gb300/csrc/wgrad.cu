@@ -264,13 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
                                tsf, tsf + 8, (c | kb) != 0);
             }
           }
-          const int cur = stage;
+          // release the stage as soon as its MMAs are issued, then prepare the next one
+          mma_commit(bar_empty(stage));
           if (++stage == kStages) stage = 0, phase ^= 1u;
           if (c + 1 < nch && !stage_scales(stage, phase)) {
             ok = false;
             break;
           }
-          mma_commit(bar_empty(cur));
         }
         if (!ok) break;
         mma_commit(bar_acc_full);

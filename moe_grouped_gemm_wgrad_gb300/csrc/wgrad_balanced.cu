@@ -377,13 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_balanced_kernel(con
                                tsf, tsf + 8, (c != x.c0 || kb != 0) ? 1u : 0u);
             }
           }
-          const int cur = stage;
+          // release the stage as soon as its MMAs are issued, then prepare the next one
+          mma_commit(bar_empty(stage));
           if (++stage == kStages) stage = 0, phase ^= 1u;
           if (c + 1 < x.c1 && !stage_scales(stage, phase)) {
             ok = false;
             break;
           }
-          mma_commit(bar_empty(cur));
         }
         if (!ok) break;
         mma_commit(bar_acc_full);
