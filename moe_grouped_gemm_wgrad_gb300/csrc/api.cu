@@ -311,6 +311,11 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
   mgw_status st = current_device(&dev);
   if (st != MGW_OK) return st;
   mgw::DgradArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!make_map_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W, in_f,
+                   static_cast<uint64_t>(E) * out_f, static_cast<uint64_t>(in_f) * 4, 256, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MGW_ERR_CUDA;
   a.dy = dy;
   a.W = W;
   a.expert_off = expert_off;

@@ -14,18 +14,21 @@
 // accuracy from Tensor Cores while surpassing the FP32 theoretical peak
 // performance", IJHPCA 2022).
 //
-// Roles (416 threads):
-//   warps 0-3   epilogue: TMEM lane quarter = warp, 32-column chunks -> fp32
-//               stores of the rows that belong to the item's expert.
-//   warp 4      MMA issuer: per 32-wide reduction chunk, 4 K-steps x 3
-//               tcgen05.mma.kind::tf32 (M=128, N=256, K=8) into one of two TMEM
-//               accumulators (2 x 256 columns), so the epilogue of one item
-//               overlaps the main loop of the next.
-//   warps 5-12  transform: load dy and W tiles from global memory one chunk ahead
-//               (software pipelined in registers; the chunk after that is prefetched
-//               into L2), split into hi/lo, write K-major
-//               128B-swizzled tiles (W transposed on the fly) into a 2-stage
-//               shared-memory ring.
+// Data path per 32-wide reduction chunk:
+//   * W[e] rows n (32 of them, 256 k columns) arrive raw by TMA into a two-stage ring;
+//   * the transform warps split them into hi/lo and write the MMA's B operand transposed
+//     (K-major, 128B-swizzled) into a two-stage shared-memory ring, and split the chunk's
+//     dy rows (loaded straight into registers) into hi/lo A operands that they store into
+//     TMEM with tcgen05.st, so A never occupies shared memory;
+//   * the MMA thread issues 4 K-steps x 3 tcgen05.mma.kind::tf32 (M=128, N=256, K=8)
+//     with A from TMEM and B from shared memory into one 256-column accumulator.
+//
+// Roles (448 threads):
+//   warps 0-3   epilogue: TMEM lane quarter = warp, 32-column chunks -> fp32 stores of
+//               the rows that belong to the item's expert, then the accumulator is free.
+//   warp 4      MMA issuer.
+//   warps 5-12  transform (two warps per TMEM lane quarter for the A operand).
+//   warp 13     TMA producer of the raw W tiles.
 #include <cstdint>
 
 #include "common.cuh"
@@ -38,20 +41,24 @@ constexpr int BM = 128;  // rows per tile (MMA M)
 constexpr int BN = 256;  // dx columns per tile (MMA N)
 constexpr int BK = 32;   // reduction (out_features) per stage: one 128-byte row of fp32
 constexpr int kStages = 2;
-constexpr int kATile = BM * BK * 4;                 // 16 KB
-constexpr int kBTile = BN * BK * 4;                 // 32 KB
-constexpr int kStageBytes = 2 * kATile + 2 * kBTile;  // A_hi, A_lo, B_hi, B_lo = 96 KB
-constexpr int kOffBar = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 4 + 1;  // full[], empty[], acc_full[2], acc_empty[2], done
+constexpr int kRawStages = 2;
+constexpr int kBTile = BN * BK * 4;             // 32 KB (hi or lo)
+constexpr int kStageBytes = 2 * kBTile;         // B_hi, B_lo = 64 KB
+constexpr int kRawBytes = BK * BN * 4;          // raw W rows: 32 x 256 fp32 = 32 KB
+constexpr int kOffRaw = kStages * kStageBytes;  // 128 KB
+constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
+// full[], empty[], raw_full[], raw_empty[], acc_full, acc_empty, done
+constexpr int kNumBars = 2 * kStages + 2 * kRawStages + 3;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffTable = kOffMisc + 16;
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
+constexpr int kXfWarp0 = 5;
 constexpr int kXfWarps = 8;
-constexpr int kThreads = (kEpiWarps + 1 + kXfWarps) * 32;
+constexpr int kTmaWarp = 13;
+constexpr int kThreads = 14 * 32;
 constexpr uint32_t kTmemCols = 512;
-// Chunks between the one loaded into registers and the one prefetched into L2.
-constexpr int kPrefetchAhead = 1;
+constexpr uint32_t kACol0 = 256;  // A operand slots: stage s hi at 256 + 64s, lo at +32
 
 __host__ __device__ constexpr size_t dgrad_smem_bytes(int E) {
   return static_cast<size_t>(kOffTable) + sizeof(int) * (3 * static_cast<size_t>(E) + 3) + 1024;
@@ -64,21 +71,40 @@ __device__ __forceinline__ uint32_t tf32_rna(float x) {
   return r;
 }
 
-__device__ __forceinline__ void split4(const float4& v, uint4& hi, uint4& lo) {
-  hi.x = tf32_rna(v.x);
-  hi.y = tf32_rna(v.y);
-  hi.z = tf32_rna(v.z);
-  hi.w = tf32_rna(v.w);
-  lo.x = tf32_rna(v.x - __uint_as_float(hi.x));
-  lo.y = tf32_rna(v.y - __uint_as_float(hi.y));
-  lo.z = tf32_rna(v.z - __uint_as_float(hi.z));
-  lo.w = tf32_rna(v.w - __uint_as_float(hi.w));
+__device__ __forceinline__ void split1(float v, uint32_t& hi, uint32_t& lo) {
+  hi = tf32_rna(v);
+  lo = tf32_rna(v - __uint_as_float(hi));
 }
 
-__device__ __forceinline__ void st_shared_u4(uint32_t addr, const uint4& v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::tf32 (A: M rows in TMEM lanes, K in columns).
+__device__ __forceinline__ void mma_tf32_at(uint32_t d, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -129,20 +155,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
   const uint32_t bar0 = sbase + kOffBar;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
   auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto bar_acc_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto bar_acc_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t bar_done = bar0 + 8u * (2 * kStages + 4);
+  auto bar_raw_full = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+  auto bar_raw_empty = [&](int s) { return bar0 + 8u * (2 * kStages + kRawStages + s); };
+  const uint32_t bar_acc_full = bar0 + 8u * (2 * kStages + 2 * kRawStages);
+  const uint32_t bar_acc_empty = bar_acc_full + 8u;
+  const uint32_t bar_done = bar_acc_full + 16u;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full(s), kXfWarps);
       mbar_init(bar_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_acc_full(b), 1);
-      mbar_init(bar_acc_empty(b), kEpiWarps);
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(bar_raw_full(s), 1);
+      mbar_init(bar_raw_empty(s), kXfWarps);
     }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, kEpiWarps);
     mbar_init(bar_done, 1);
     fence_mbar_init();
+    tma_prefetch_desc(&args.tm_w);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&s_misc[0]), kTmemCols);
@@ -157,135 +188,104 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
   const long long total = static_cast<long long>(s_rtp[E]) * tiles_k;
   const int nchunks = out_f / BK;
 
-  if (warp >= kEpiWarps + 1) {
-    // ----------------------------------------------------------- transform
-    // Software-pipelined: the global loads of the next chunk (possibly of the next item)
-    // are in flight while the current chunk is split and written to shared memory.
-    const int xt = tid - (kEpiWarps + 1) * 32;  // 0..255
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    // raw operands of one chunk in registers: dy 4 x float4, W 8 x 4 floats
-    struct Raw {
-      float4 a[4];
-      float b[8][4];
-    };
-    auto load_chunk = [&](const Item& item, int c, Raw& raw) {
-      const int row0 = s_off[item.e] + item.rt * BM;
-      const int valid = min(BM, s_off[item.e + 1] - row0);
-      // A = dy[row0 .. row0+127, 32c .. 32c+31]: 128 rows x 8 chunks of 16 B.
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int idx = xt + p * 256;
-        const int r = idx >> 3, j = idx & 7;
-        raw.a[p] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < valid)
-          raw.a[p] = __ldg(reinterpret_cast<const float4*>(
-              args.dy + static_cast<size_t>(row0 + r) * out_f + c * BK + 4 * j));
-      }
-      // B^T tile: dx column k (K-major row k of B) and 4 consecutive n; lane -> k.
-      const float* Wk = args.W + static_cast<size_t>(item.e) * out_f * in_f + item.kt * BN;
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const int idx = xt + p * 256;            // 0..2047
-        const int k = idx & 255, ng = idx >> 8;  // ng in 0..7
-        const float* src = Wk + static_cast<size_t>(c * BK + 4 * ng) * in_f + k;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) raw.b[p][q] = __ldg(src + static_cast<size_t>(q) * in_f);
-      }
-    };
-    // L2 prefetch of a chunk: its 32 W row segments (8 lines each) and 128 dy row segments
-    // (one line each), 384 lines over 256 threads, so that the register loads one chunk
-    // later hit L2 instead of waiting on DRAM.
-    auto prefetch_chunk = [&](const Item& item, int c) {
-      const int row0 = s_off[item.e] + item.rt * BM;
-      const int valid = min(BM, s_off[item.e + 1] - row0);
-      const float* Wk = args.W + static_cast<size_t>(item.e) * out_f * in_f + item.kt * BN;
-      for (int i = xt; i < 384; i += 256) {
-        const float* p;
-        if (i < 256) {
-          p = Wk + static_cast<size_t>(c * BK + (i >> 3)) * in_f + (i & 7) * 32;
-        } else {
-          const int r = i - 256;
-          if (r >= valid) continue;
-          p = args.dy + static_cast<size_t>(row0 + r) * out_f + c * BK;
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------- raw W tiles by TMA
+    if (lane == 0) {
+      int rs = 0;
+      uint32_t rph = 0;
+      int pending[kRawStages];
+      uint32_t pending_phase[kRawStages];
+      for (int s = 0; s < kRawStages; ++s) pending[s] = 0, pending_phase[s] = 0;
+      bool ok = true;
+      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const Item item = decode_item(it, tiles_k, s_rtp, E);
+        for (int c = 0; c < nchunks; ++c) {
+          if (!mbar_wait(bar_raw_empty(rs), rph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_raw_full(rs);
+          mbar_arrive_expect_tx(fb, kRawBytes);
+          tma_load_2d(sbase + kOffRaw + rs * kRawBytes, &args.tm_w, item.kt * BN,
+                      item.e * out_f + c * BK, fb);
+          pending[rs] = 1;
+          pending_phase[rs] = rph;
+          if (++rs == kRawStages) rs = 0, rph ^= 1u;
         }
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
       }
-    };
-    // (item, c) -> the chunk after it in this CTA's sequence; false past the last
-    auto advance = [&](long long& it2, Item& item2, int& c2) -> bool {
-      if (++c2 == nchunks) {
-        c2 = 0;
-        it2 += gridDim.x;
-        if (it2 >= total) return false;
-        item2 = decode_item(it2, tiles_k, s_rtp, E);
+      if (!ok) {
+        *abort_flag = 1;
+        if (args.status) atomicOr(args.status, kDevTimeout);
       }
-      return true;
-    };
-    long long it = blockIdx.x;
-    Raw cur, nxt;
-    Item item{0, 0, 0};
-    int c = 0;
-    if (it < total) {
-      item = decode_item(it, tiles_k, s_rtp, E);
-      load_chunk(item, 0, cur);
+      for (int s = 0; s < kRawStages; ++s)
+        if (pending[s]) mbar_wait_drain(bar_raw_full(s), pending_phase[s]);
     }
-    while (it < total && ok) {
-      // the chunk after (item, c): next chunk of this item, else chunk 0 of the next item
-      long long nit = it;
-      int nc = c + 1;
-      Item nitem = item;
-      if (nc == nchunks) {
-        nc = 0;
-        nit = it + gridDim.x;
-        if (nit < total) nitem = decode_item(nit, tiles_k, s_rtp, E);
-      }
-      if (nit < total) {
-        load_chunk(nitem, nc, nxt);
-        long long pit = nit;
-        Item pitem = nitem;
-        int pc = nc;
-        bool more = true;
-        for (int d = 0; d < kPrefetchAhead && more; ++d) more = advance(pit, pitem, pc);
-        if (more) prefetch_chunk(pitem, pc);
-      }
-      if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint32_t s_ahi = sbase + stage * kStageBytes;
-      const uint32_t s_alo = s_ahi + kATile;
-      const uint32_t s_bhi = s_alo + kATile;
-      const uint32_t s_blo = s_bhi + kBTile;
+  } else if (warp >= kXfWarp0) {
+    // ----------------------------------------------------------- transform
+    const int xw = warp - kXfWarp0;            // 0..7
+    const int xt = tid - kXfWarp0 * 32;        // 0..255: the B row k of this thread
+    const uint32_t q = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter for A
+    const int kh = xw >> 2;                    // A columns 16*kh .. 16*kh+15 of the chunk
+    int stage = 0, rs = 0;
+    uint32_t phase = 0, rph = 0;
+    bool ok = true;
+    for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      const Item item = decode_item(it, tiles_k, s_rtp, E);
+      const int row0 = s_off[item.e] + item.rt * BM;
+      const int valid = min(BM, s_off[item.e + 1] - row0);
+      const int r = static_cast<int>(q) * 32 + static_cast<int>(lane);  // this thread's A row
+      const float* dyrow = args.dy + static_cast<size_t>(row0 + (r < valid ? r : 0)) * out_f + 16 * kh;
+      for (int c = 0; c < nchunks; ++c) {
+        // A: 16 consecutive reduction elements of row r, straight from global memory
+        float4 a4[4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int idx = xt + p * 256;
-        const int r = idx >> 3, j = idx & 7;
-        uint4 hi, lo;
-        split4(cur.a[p], hi, lo);
-        const uint32_t off = r * 128 + ((j ^ (r & 7)) << 4);
-        st_shared_u4(s_ahi + off, hi);
-        st_shared_u4(s_alo + off, lo);
-      }
+        for (int j = 0; j < 4; ++j) {
+          a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (r < valid) a4[j] = __ldg(reinterpret_cast<const float4*>(dyrow + c * BK) + j);
+        }
+        if (!mbar_wait(bar_raw_full(rs), rph, abort_flag) ||
+            !mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // B: row k = xt of the K-major tile holds W[n][k] for the chunk's 32 n; thread xt reads
+        // column k of the raw [32 n][256 k] tile (conflict-free) and writes 8 x 16 bytes
+        const float* raw = reinterpret_cast<const float*>(smem + kOffRaw + rs * kRawBytes);
+        const uint32_t s_bhi = sbase + stage * kStageBytes;
+        const uint32_t s_blo = s_bhi + kBTile;
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const int idx = xt + p * 256;
-        const int k = idx & 255, ng = idx >> 8;
-        uint4 hi, lo;
-        split4(make_float4(cur.b[p][0], cur.b[p][1], cur.b[p][2], cur.b[p][3]), hi, lo);
-        const uint32_t off = k * 128 + ((ng ^ (k & 7)) << 4);
-        st_shared_u4(s_bhi + off, hi);
-        st_shared_u4(s_blo + off, lo);
+        for (int ng = 0; ng < 8; ++ng) {
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) split1(raw[(4 * ng + j) * BN + xt], h[j], l[j]);
+          const uint32_t off = xt * 128 + ((ng ^ (xt & 7)) << 4);
+          st_shared_u4(s_bhi + off, h[0], h[1], h[2], h[3]);
+          st_shared_u4(s_blo + off, l[0], l[1], l[2], l[3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_raw_empty(rs));
+        if (++rs == kRawStages) rs = 0, rph ^= 1u;
+        // A hi/lo into this stage's TMEM slot, this warp's lane quarter and column half
+        {
+          uint32_t ah[16], al[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            split1(a4[j].x, ah[4 * j], al[4 * j]);
+            split1(a4[j].y, ah[4 * j + 1], al[4 * j + 1]);
+            split1(a4[j].z, ah[4 * j + 2], al[4 * j + 2]);
+            split1(a4[j].w, ah[4 * j + 3], al[4 * j + 3]);
+          }
+          const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 64u * stage + 16u * kh;
+          tmem_st_x16(ta, ah);
+          tmem_st_x16(ta + 32, al);
+          tmem_wait_st();
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_full(stage));
+        if (++stage == kStages) stage = 0, phase ^= 1u;
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_full(stage));
-      if (++stage == kStages) stage = 0, phase ^= 1u;
-      it = nit;
-      c = nc;
-      item = nitem;
-      cur = nxt;
     }
     if (!ok) {
       *abort_flag = 1;
@@ -295,44 +295,38 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_phase[2] = {0u, 0u};
-      int local = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       constexpr uint32_t idesc = idesc_tf32(BM, BN);
-      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
-      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x, ++local) {
-        const int b = local & 1;
-        if (!mbar_wait_spin(bar_acc_empty(b), acc_phase[b] ^ 1u, abort_flag)) {
+      const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase);
+      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        if (!mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        acc_phase[b] ^= 1u;
+        acc_phase ^= 1u;
         tc_fence_after();
-        const uint32_t dacc = tmem + 256u * b;
         for (int c = 0; c < nchunks; ++c) {
           if (!mbar_wait_spin(bar_full(stage), phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // descriptors from one base: tiles and the 32-byte K steps are offsets / 16 in the
-          // start-address field (the ring lies below 256 KB: no carry)
-          const uint64_t ahi = a_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
-          const uint64_t alo = ahi + (kATile >> 4);
-          const uint64_t bhi = alo + (kATile >> 4);
+          const uint64_t bhi = b_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
           const uint64_t blo = bhi + (kBTile >> 4);
+          const uint32_t ahi = tmem + kACol0 + 64u * stage;
+          const uint32_t alo = ahi + 32u;
 #pragma unroll
           for (int ks = 0; ks < BK / 8; ++ks) {
-            mma_tf32(dacc, alo + 2 * ks, bhi + 2 * ks, idesc, (c | ks) != 0);
-            mma_tf32(dacc, ahi + 2 * ks, blo + 2 * ks, idesc, 1u);
-            mma_tf32(dacc, ahi + 2 * ks, bhi + 2 * ks, idesc, 1u);
+            mma_tf32_at(tmem, alo + 8u * ks, bhi + 2 * ks, idesc, (c | ks) != 0);
+            mma_tf32_at(tmem, ahi + 8u * ks, blo + 2 * ks, idesc, 1u);
+            mma_tf32_at(tmem, ahi + 8u * ks, bhi + 2 * ks, idesc, 1u);
           }
           mma_commit(bar_empty(stage));
           if (++stage == kStages) stage = 0, phase ^= 1u;
         }
         if (!ok) break;
-        mma_commit(bar_acc_full(b));
+        mma_commit(bar_acc_full);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -344,24 +338,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp;  // warps 0-3
-    uint32_t acc_phase[2] = {0u, 0u};
-    int local = 0;
-    for (long long it = blockIdx.x; it < total; it += gridDim.x, ++local) {
-      const int b = local & 1;
+    uint32_t acc_phase = 0;
+    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
       if (*abort_flag) break;
-      if (!mbar_wait(bar_acc_full(b), acc_phase[b], abort_flag)) {
+      if (!mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
         *abort_flag = 1;
         if (lane == 0 && args.status) atomicOr(args.status, kDevTimeout);
         break;
       }
-      acc_phase[b] ^= 1u;
+      acc_phase ^= 1u;
       tc_fence_after();
       const Item item = decode_item(it, tiles_k, s_rtp, E);
       const int row0 = s_off[item.e] + item.rt * BM;
       const int valid = min(BM, s_off[item.e + 1] - row0);
       const int r = quarter * 32 + static_cast<int>(lane);
       float* dst = args.dx + static_cast<size_t>(row0 + r) * in_f + item.kt * BN;
-      const uint32_t ta = tmem + 256u * b + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
       for (int j = 0; j < BN / 32; ++j) {
         uint32_t v[32];
@@ -369,15 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
         tmem_wait_ld();
         if (r < valid) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(dst + 32 * j + 4 * q) =
-                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          for (int qq = 0; qq < 8; ++qq)
+            *reinterpret_cast<float4*>(dst + 32 * j + 4 * qq) =
+                make_float4(__uint_as_float(v[4 * qq]), __uint_as_float(v[4 * qq + 1]),
+                            __uint_as_float(v[4 * qq + 2]), __uint_as_float(v[4 * qq + 3]));
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_acc_empty(b));
+      if (lane == 0) mbar_arrive(bar_acc_empty);
     }
   }
 

@@ -89,6 +89,7 @@ struct MmArgs {
 cudaError_t launch_grouped_mm_mxfp8(const MmArgs& a, int num_sms, cudaStream_t stream);
 
 struct DgradArgs {
+  CUtensorMap tm_w;    // W fp32 [E*out_f, in_f], box 256 columns x 32 rows, no swizzle
   const float* dy;
   const float* W;
   const int32_t* expert_off;
