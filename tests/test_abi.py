@@ -123,3 +123,15 @@ def test_argument_errors_noalloc_wgrad(lib):
         None, fake, fake, fake, fake, 1, 4, 128, 256, 256, fake, None, None) == -1
     assert lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc(
         fake, fake, fake, fake, fake, 513, 4, 128, 256, 1 << 17, fake, None, None) == -2
+
+
+def test_workspace_size_helper(lib):
+    import torch
+
+    n = lib.mgw_grouped_wgrad_workspace_bytes(8, 256, 256)
+    if torch.cuda.is_available():
+        # header + tile counters (padded to 256 bytes) + 2 x SM count partial tiles of 128 KB
+        slots = 2 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        assert n == 256 + (4 * slots + 255) // 256 * 256 + slots * 128 * 256 * 4
+    else:
+        assert n == 0

@@ -1,0 +1,41 @@
+"""The benchmark's JSON contract on CPU: the reference arm (the oracle, timed on the host) prints
+one line with the metric, unit and direction of the GPU arm, its CPU-baseline description and an
+end-to-end object with zero transfer bytes; non-zero ranks of a multi-rank launch print nothing."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(args, env=None):
+    e = dict(os.environ)
+    if env:
+        e.update(env)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT,
+                         capture_output=True, text=True, timeout=600, env=e)
+    assert out.returncode == 0, out.stderr[-2000:]
+    return [ln for ln in out.stdout.splitlines() if ln.strip()]
+
+
+def test_reference_arm_line():
+    lines = _run(["--impl", "reference", "--workload", "wgrad_tiny", "--steps", "2", "--warmup", "1"])
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == "MXFP8 grouped wgrad TFLOP/s" and d["unit"] == "TFLOP/s"
+    assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["dtype"] == "f64" and d["data"] == "synthetic"
+    assert d["config"]["workload"] == "wgrad_tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    lines = _run(["--impl", "reference", "--workload", "wgrad_tiny", "--steps", "1", "--warmup", "0"],
+                 env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert lines == []
