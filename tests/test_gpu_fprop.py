@@ -301,3 +301,25 @@ def test_moe_ffn_pair_forward_and_mx_dgrad_full_size_sampled():
             got.append(dxs[r, k])
     refs, got = np.array(refs), np.array(got)
     assert (np.abs(got - refs) <= wgrad_tol(refs, float(np.sqrt(np.mean(refs ** 2))))).all()
+
+
+def test_forward_and_mx_dgrad_max_experts():
+    """1024 experts (the library's limit), most with no rows, a few ragged: parity of the
+    row-wise quantizer and both GEMMs on every output element."""
+    rng = np.random.default_rng(91)
+    counts = np.zeros(1024, dtype=np.int64)
+    counts[[0, 5, 511, 1023]] = [40, 1, 130, 7]
+    N, K = 256, 256
+    x, W, off, w_off = _fprop_case(list(counts), N, K, seed=92)
+    _assert_rows_exact(x, off)
+    y, _, _ = _run_fprop(x, W, off, w_off, N)
+    xq, xs = oracle.mxfp8_quantize_rows(x, off)
+    wq, ws = oracle.mxfp8_quantize_rows(W, w_off)
+    ref = oracle.grouped_fprop_mx(xq, xs, wq, ws, off, w_off, x.shape[0])
+    assert (np.abs(bf16_to_f64(y) - ref) <= wgrad_tol(ref)).all()
+    dy, W2, off2, w_off2 = _dgrad_case(list(counts), 128, 256, seed=93)
+    dx, _, _ = _run_dgrad_mx(dy, W2, off2, w_off2)
+    dyq, dys = oracle.mxfp8_quantize_rows(dy, off2)
+    wtq, wts = oracle.mxfp8_quantize(W2, w_off2)
+    ref2 = oracle.grouped_dgrad_mx(dyq, dys, wtq, wts, off2, w_off2, dy.shape[0])
+    assert (np.abs(bf16_to_f64(dx) - ref2) <= wgrad_tol(ref2)).all()

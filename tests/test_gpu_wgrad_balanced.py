@@ -158,3 +158,11 @@ def test_balanced_skewed_workload_full_size_sampled(ws):
     empty = torch.as_tensor(np.nonzero(counts == 0)[0], device="cuda")
     assert not bool(full[empty].float().abs().amax())
     assert _counters_zero(ws)
+
+
+def test_balanced_max_experts(ws):
+    """512 experts (the balanced kernel's limit): mostly empty, one long enough to be split."""
+    counts = np.zeros(512, dtype=np.int64)
+    counts[[3, 100, 400, 511]] = [2000, 33, 129, 1]
+    case = synth.wgrad_random(int(counts.sum()), 128, 256, counts, seed=52)
+    _check_full(case, ws)
