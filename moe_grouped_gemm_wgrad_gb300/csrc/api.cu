@@ -180,6 +180,8 @@ mgw_status wgrad_check(const void* gq, const void* gs, const void* xq, const voi
   if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > MGW_MAX_EXPERTS) return MGW_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 256 != 0) return MGW_ERR_UNSUPPORTED;
   if (static_cast<long long>(E) * N > (1ll << 31)) return MGW_ERR_UNSUPPORTED;
+  // output tiles (128 x 256) must be countable in 32 bits
+  if (static_cast<long long>(E) * (N / 128) * (K / 256) >= (1ll << 31)) return MGW_ERR_UNSUPPORTED;
   if (Mcap % 128 != 0 || Mcap < mgw_mxfp8_token_capacity(M, E) || Mcap > (size_t(1) << 31))
     return MGW_ERR_CAPACITY;
   if (!aligned16(gq) || !aligned16(xq) || !aligned16(gs) || !aligned16(xs) || !aligned16(out_bf16))

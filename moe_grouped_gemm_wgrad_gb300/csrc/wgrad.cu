@@ -157,8 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
   const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
 
   const int tiles_n = N / BM, tiles_k = K / BN;
-  const long long per_expert = static_cast<long long>(tiles_n) * tiles_k;
-  const long long total = per_expert * E;
+  // Item indices fit in 32 bits (the C ABI checks E x tiles < 2^31), so the per-item decode
+  // uses 32-bit divisions: the MMA thread runs it once per item.
+  const int per_expert = tiles_n * tiles_k;
+  const long long total = static_cast<long long>(per_expert) * E;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -172,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
       long long it = 0;
       while (ok && items.next(it)) {
-        const int e = s_order[it / per_expert];
-        const int tile = static_cast<int>(it % per_expert);
+        const int e = s_order[static_cast<int>(it) / per_expert];
+        const int tile = static_cast<int>(it) % per_expert;
         const int nt = tile / tiles_k, kt = tile % tiles_k;
         const int cnt = s_off[e + 1] - s_off[e];
         if (cnt == 0) continue;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
       ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
       long long it = 0;
       while (ok && items.next(it)) {
-        const int e = s_order[it / per_expert];
+        const int e = s_order[static_cast<int>(it) / per_expert];
         const int cnt = s_off[e + 1] - s_off[e];
         if (cnt == 0) continue;
         const int nch = (cnt + BT - 1) / BT;
@@ -293,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
     ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
     long long it = 0;
     while (items.next(it)) {
-      const int e = s_order[it / per_expert];
+      const int e = s_order[static_cast<int>(it) / per_expert];
       if (s_off[e + 1] != s_off[e]) continue;
-      const int tile = static_cast<int>(it % per_expert);
+      const int tile = static_cast<int>(it) % per_expert;
       const int nt = tile / tiles_k, kt = tile % tiles_k;
       uint8_t* base = out + (static_cast<size_t>(e) * N + nt * BM) * pitch +
                       static_cast<size_t>(kt) * BN * 2 + lane * 16;
@@ -314,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
     ItemIter items{total, gridDim.x, 0, static_cast<int>(blockIdx.x)};
     long long it = 0;
     while (items.next(it)) {
-      const int e = s_order[it / per_expert];
-      const int tile = static_cast<int>(it % per_expert);
+      const int e = s_order[static_cast<int>(it) / per_expert];
+      const int tile = static_cast<int>(it) % per_expert;
       const int nt = tile / tiles_k, kt = tile % tiles_k;
       const int cnt = s_off[e + 1] - s_off[e];
       if (cnt == 0) continue;  // written by the zero warp
