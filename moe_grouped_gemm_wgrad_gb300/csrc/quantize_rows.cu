@@ -43,7 +43,7 @@ __device__ __forceinline__ uint32_t abs_max_bf16x2(uint32_t m, uint32_t w) {
   return max(m, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));  // |bf16| orders like its bits
 }
 
-__global__ void __launch_bounds__(kRThreads) mxfp8_quantize_rows_kernel(
+__global__ void __launch_bounds__(kRThreads, 4) mxfp8_quantize_rows_kernel(
     const uint16_t* __restrict__ src, int src_rows, const int32_t* __restrict__ row_index, int M,
     int C, const int32_t* __restrict__ expert_off, int E, uint8_t* __restrict__ q,
     uint8_t* __restrict__ sc, long long Mcap, int rule, int* status) {
