@@ -79,6 +79,8 @@ def _load():
             lib.orc_grouped_dgrad.restype = None
             lib.orc_grouped_dgrad_element.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
             lib.orc_grouped_dgrad_element.restype = dbl
+            lib.orc_grouped_dgrad_page_f32.argtypes = [P, P, P, i32, i32, i32, i32, i32, P]
+            lib.orc_grouped_dgrad_page_f32.restype = None
             lib.orc_mxfp8_quantize_rows.argtypes = [P, i32, i32, P, i32, i64, i32, P, P]
             lib.orc_mxfp8_quantize_rows.restype = None
             lib.orc_mx_dot.argtypes = [P, P, P, P, i32]
@@ -220,6 +222,21 @@ def grouped_dgrad_element(dy: np.ndarray, W: np.ndarray, expert_off, r: int, k: 
     v = _load().orc_grouped_dgrad_element(_ptr(dy), _ptr(W), _ptr(off), E, rows, out_f, in_f,
                                           r, k, ctypes.c_void_p(ctypes.addressof(b)))
     return v, b.value
+
+
+def grouped_dgrad_page_f32(dy: np.ndarray, W: np.ndarray, expert_off, fused: bool = True):
+    """The dgrad page's fp32 formulation (32-row groups, running fp32 sums over the
+    output features; fused multiply-add or product-then-add).  A cross-check of
+    :func:`grouped_dgrad`, not the definition.  Returns fp32 dx [rows, in_f]."""
+    dy = np.ascontiguousarray(dy, dtype=np.float32)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    off = _off(expert_off)
+    rows, out_f = dy.shape
+    E, _, in_f = W.shape
+    dx = np.empty((rows, in_f), dtype=np.float32)
+    _load().orc_grouped_dgrad_page_f32(_ptr(dy), _ptr(W), _ptr(off), E, rows, out_f, in_f,
+                                       1 if fused else 0, _ptr(dx))
+    return dx
 
 
 # ------------------------------------------- forward and data-gradient GEMMs (MXFP8)

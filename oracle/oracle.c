@@ -252,6 +252,41 @@ void orc_grouped_dgrad(const float *dy, const float *W, const int32_t *off, int 
     }
 }
 
+/* The dgrad page's own fp32 formulation, restated as a cross-check of the fp64
+ * definition above (it is not the definition).  Rows are taken in groups of 32.  A
+ * group whose first and last rows map to the same expert multiplies all its rows by that
+ * expert's weights; a group that straddles an expert boundary looks up each row's expert
+ * on its own.  Each output is a running fp32 sum over the output features in order; the
+ * page's shared-memory tiling of n and k does not change that order.  The page leaves
+ * open whether a product is fused into the sum, so both readings are offered:
+ * fused != 0 takes fmaf, fused == 0 rounds the product first. */
+void orc_grouped_dgrad_page_f32(const float *dy, const float *W, const int32_t *off, int E,
+                                int rows, int out_f, int in_f, int fused, float *dx) {
+  for (int base = 0; base < rows; base += 32) {
+    const int end = base + 32 < rows ? base + 32 : rows;
+    const int e_first = orc_expert_for_row_scan(off, E, base);
+    const int e_last = orc_expert_for_row_scan(off, E, end - 1);
+    for (int r = base; r < end; ++r) {
+      const int e = e_first == e_last ? e_first : orc_expert_for_row_scan(off, E, r);
+      const float *a = dy + (int64_t)r * out_f;
+      const float *w = W + (int64_t)e * out_f * in_f;
+      for (int k = 0; k < in_f; ++k) {
+        float sum = 0.0f;
+        for (int n = 0; n < out_f; ++n) {
+          const float wv = w[(int64_t)n * in_f + k];
+          if (fused) {
+            sum = fmaf(a[n], wv, sum);
+          } else {
+            const float prod = a[n] * wv;
+            sum = sum + prod;
+          }
+        }
+        dx[(int64_t)r * in_f + k] = sum;
+      }
+    }
+  }
+}
+
 /* ------------------------------------------- forward and data-gradient GEMMs */
 
 /* The post-attn page stages every routed token's activations for its expert GEMMs as

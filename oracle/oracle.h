@@ -76,6 +76,13 @@ void orc_grouped_dgrad(const float *dy, const float *W, const int32_t *off, int 
 double orc_grouped_dgrad_element(const float *dy, const float *W, const int32_t *off, int E,
                                  int rows, int out_f, int in_f, int r, int k, double *bound_out);
 
+/* The dgrad page's fp32 formulation (32-row groups; a group within one expert takes
+ * that expert's weights, a straddling group looks up each row; running fp32 sums over
+ * n in order, fused multiply-add when fused != 0).  A cross-check of orc_grouped_dgrad,
+ * which any correct result must match within 1e-5 * bound. */
+void orc_grouped_dgrad_page_f32(const float *dy, const float *W, const int32_t *off, int E,
+                                int rows, int out_f, int in_f, int fused, float *dx);
+
 /* ----------------------------------------------- forward and data-gradient GEMMs
  * MXFP8 operands quantized along the hidden (contraction) axis of each row. */
 

@@ -257,6 +257,32 @@ def test_dgrad_single_expert_is_dense_gemm():
                                rtol=1e-12, atol=1e-12)
 
 
+# Offsets 0,7,7,47,48,48,148: rows 0-31 and 32-63 straddle expert boundaries (each row
+# looks up its own expert), rows 64-147 fall in 32-row groups of one expert.
+@pytest.mark.parametrize("counts,out_f,in_f,seed", [
+    ([7, 0, 40, 1, 0, 100], 48, 20, 21),
+    ([64, 32, 0, 33], 1536, 8, 22),   # long sums: the MoE FFN pair's 1536 output features
+    ([200], 64, 16, 23),              # one expert: every group takes the shortcut
+])
+def test_dgrad_page_fp32_formulation_within_tolerance(counts, out_f, in_f, seed):
+    """The dgrad page's own fp32 arithmetic (group shortcut, sequential fp32 sums, fused or
+    not) lands within 1e-5 * sum|dy||W| of the fp64 definition: the tolerance admits the
+    page's result, and an indexing slip in either formulation would not."""
+    case = synth.dgrad_random(sum(counts), out_f, in_f, counts, seed=seed)
+    dx, bound = oracle.grouped_dgrad(case.dy, case.W, case.expert_off)
+    for fused in (True, False):
+        got = oracle.grouped_dgrad_page_f32(case.dy, case.W, case.expert_off, fused)
+        assert got.dtype == np.float32 and got.shape == dx.shape
+        err = np.abs(got.astype(np.float64) - dx)
+        assert np.all(err <= 1e-5 * bound), float((err / np.maximum(bound, 1e-300)).max())
+    # Rows of the straddling groups differ from what the group's first expert would give.
+    if len(counts) > 1:
+        off = case.expert_off
+        r = int(off[1])  # first row after expert 0
+        wrong = case.dy[r].astype(np.float64) @ case.W[0].astype(np.float64)
+        assert np.abs(wrong - dx[r]).max() > 1e-3 * np.abs(dx[r]).max()
+
+
 # ------------------------------------------------------ RoundUp scale rule
 def test_ceil448_scale_golden_and_bracket():
     g = _golden("e4m3_e8m0_examples.json")["scale_byte_ceil448"]
