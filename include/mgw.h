@@ -215,7 +215,9 @@ size_t mgw_grouped_wgrad_workspace_bytes(int E, int N, int K);
  * W          device, fp32 [E, out_f, in_f] row-major (in_f contiguous), the dgrad
  *            page's weight layout W[(e*out_f + n)*in_f + k].
  * expert_off device int32 [E+1], 0 = off[0] <= ... <= off[E] = rows.
- * rows >= 0; out_f a positive multiple of 32; in_f a positive multiple of 256.
+ * rows >= 0; out_f a positive multiple of 32; in_f a positive multiple of 256;
+ * E * out_f < 2^31 (the stacked weight rows are addressed with 32-bit
+ * coordinates; else MGW_ERR_UNSUPPORTED).
  * dx         device, fp32 [rows, in_f] row-major, fully written.
  * status_dev device int, nullable.
  */

@@ -307,6 +307,8 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
   if (rows < 0 || out_f <= 0 || in_f <= 0 || E < 1 || E > MGW_MAX_EXPERTS)
     return MGW_ERR_INVALID_ARG;
   if (out_f % 32 != 0 || in_f % 256 != 0) return MGW_ERR_UNSUPPORTED;
+  // stacked weight rows e*out_f + n are TMA coordinates (32-bit)
+  if (static_cast<long long>(E) * out_f >= (1ll << 31)) return MGW_ERR_UNSUPPORTED;
   if ((dy && !aligned16(dy)) || !aligned16(W) || (dx && !aligned16(dx)))
     return MGW_ERR_INVALID_ARG;
   DeviceInfo dev;

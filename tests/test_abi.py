@@ -71,6 +71,8 @@ def test_argument_errors_before_device_work(lib):
     assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1, 4, 32, 128, fake, None, None) == -2
     assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1, 4, 48, 256, fake, None, None) == -2
     assert lib.mgw_grouped_dgrad_f32(fake, None, fake, 1, 4, 32, 256, fake, None, None) == -1
+    # stacked weight rows E * out_f must stay below 2^31
+    assert lib.mgw_grouped_dgrad_f32(fake, fake, fake, 1024, 4, 1 << 21, 256, fake, None, None) == -2
 
 
 def test_argument_errors_forward_and_mx_dgrad(lib):
