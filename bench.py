@@ -471,11 +471,15 @@ def oracle_wgrad_sample(case, n_sub: int, k_sub: int):
     return sec, flops, f"expert {e} ({t1 - t0} tokens), grad_w block {n_sub}x{k_sub}, quantize+wgrad, 1 thread"
 
 
-def cpu_baseline(case, target_s: float = 12.0):
-    sec, flops, _ = oracle_wgrad_sample(case, 128, 128)
+def cpu_baseline(case, target_s: float = 16.0):
+    """About target_s seconds of oracle work (10-30 s on the hosts measured): a
+    1024 x 1024 pilot block, large enough that the quantization of the slice does not
+    dominate, then a square block scaled by area."""
+    pilot_n, pilot_k = min(1024, case.N), min(1024, case.K)
+    sec, _, _ = oracle_wgrad_sample(case, pilot_n, pilot_k)
     scale = max(1.0, (target_s / max(sec, 1e-3)) ** 0.5)
-    n_sub = int(min(case.N, max(128, 128 * round(scale))))
-    k_sub = int(min(case.K, max(128, 128 * round(scale))))
+    n_sub = int(min(case.N, max(128, 128 * round(pilot_n * scale / 128))))
+    k_sub = int(min(case.K, max(128, 128 * round(pilot_k * scale / 128))))
     sec, flops, desc = oracle_wgrad_sample(case, n_sub, k_sub)
     return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
             "sample": desc, "seconds": sec}
