@@ -39,3 +39,19 @@ def test_reference_arm_other_ranks_print_nothing():
     lines = _run(["--impl", "reference", "--workload", "wgrad_tiny", "--steps", "1", "--warmup", "0"],
                  env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert lines == []
+
+
+def test_cpu_baseline_sizes_its_sample_from_a_pilot():
+    """The default run's CPU baseline: the oracle on a square grad_w block whose side is a
+    multiple of 128, sized from the pilot toward the requested seconds, and described."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from moe_grouped_gemm_wgrad_gb300 import synth
+
+    case = synth.wgrad_random(2048, 1024, 1024, [1024, 1024], seed=3)
+    cb = bench.cpu_baseline(case, target_s=0.2)
+    assert cb["kind"] == "oracle" and cb["unit"] == "TFLOP/s" and cb["cores"] == 1
+    assert cb["value"] > 0 and cb["seconds"] > 0
+    side = int(cb["sample"].split("grad_w block ")[1].split("x")[0])
+    assert side % 128 == 0 and 128 <= side <= 1024
+    assert "1024 tokens" in cb["sample"]
