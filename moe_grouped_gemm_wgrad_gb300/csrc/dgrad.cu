@@ -23,12 +23,15 @@
 //   * the MMA thread issues 4 K-steps x 3 tcgen05.mma.kind::tf32 (M=128, N=256, K=8)
 //     with A from TMEM and B from shared memory into one 256-column accumulator.
 //
-// Roles (448 threads):
+// Roles (704 threads):
 //   warps 0-3   epilogue: TMEM lane quarter = warp, 32-column chunks -> fp32 stores of
 //               the rows that belong to the item's expert, then the accumulator is free.
 //   warp 4      MMA issuer.
-//   warps 5-12  transform (two warps per TMEM lane quarter for the A operand).
-//   warp 13     TMA producer of the raw W tiles.
+//   warps 5-20  transform: per chunk, thread t splits half of B row t % 256 (16 of the 32
+//               reduction elements) and 8 A elements of one row (four warps per TMEM lane
+//               quarter, 8 columns each).  Sixteen warps instead of eight halve each warp's
+//               serial chain of loads, splits and stores per chunk.
+//   warp 21     TMA producer of the raw W tiles.
 #include <cstdint>
 
 #include "common.cuh"
@@ -54,9 +57,14 @@ constexpr int kOffTable = kOffMisc + 16;
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kXfWarp0 = 5;
-constexpr int kXfWarps = 8;
-constexpr int kTmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kXfWarps = 16;
+constexpr int kXfThreads = kXfWarps * 32;
+constexpr int kBParts = kXfThreads / BN;     // threads per B row
+constexpr int kNgPer = (BK / 4) / kBParts;   // groups of 4 reduction elements per thread
+constexpr int kACols = BK / (kXfWarps / 4);  // A columns per transform warp
+constexpr int kTmaWarp = kXfWarp0 + kXfWarps;
+constexpr int kThreads = (kTmaWarp + 1) * 32;
+static_assert(kXfThreads % BN == 0 && (BK / 4) % kBParts == 0 && kACols == 8, "transform split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;  // A operand slots: stage s hi at 256 + 64s, lo at +32
 
@@ -83,13 +91,10 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
       : "memory");
 }
 
@@ -222,10 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
     }
   } else if (warp >= kXfWarp0) {
     // ----------------------------------------------------------- transform
-    const int xw = warp - kXfWarp0;            // 0..7
-    const int xt = tid - kXfWarp0 * 32;        // 0..255: the B row k of this thread
+    const int xw = warp - kXfWarp0;              // 0..15
+    const int xt = tid - kXfWarp0 * 32;          // 0..511
+    const int bk = xt % BN;                      // the B row k of this thread
+    const int ng0 = (xt / BN) * kNgPer;          // its first group of 4 reduction elements
     const uint32_t q = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter for A
-    const int kh = xw >> 2;                    // A columns 16*kh .. 16*kh+15 of the chunk
+    const int kh = xw >> 2;                      // A columns 8*kh .. 8*kh+7 of the chunk
     int stage = 0, rs = 0;
     uint32_t phase = 0, rph = 0;
     bool ok = true;
@@ -234,12 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       const int row0 = s_off[item.e] + item.rt * BM;
       const int valid = min(BM, s_off[item.e + 1] - row0);
       const int r = static_cast<int>(q) * 32 + static_cast<int>(lane);  // this thread's A row
-      const float* dyrow = args.dy + static_cast<size_t>(row0 + (r < valid ? r : 0)) * out_f + 16 * kh;
+      const float* dyrow = args.dy + static_cast<size_t>(row0 + (r < valid ? r : 0)) * out_f + kACols * kh;
       for (int c = 0; c < nchunks; ++c) {
-        // A: 16 consecutive reduction elements of row r, straight from global memory
-        float4 a4[4];
+        // A: 8 consecutive reduction elements of row r, straight from global memory
+        float4 a4[kACols / 4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kACols / 4; ++j) {
           a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (r < valid) a4[j] = __ldg(reinterpret_cast<const float4*>(dyrow + c * BK) + j);
         }
@@ -248,36 +255,38 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
           ok = false;
           break;
         }
-        // B: row k = xt of the K-major tile holds W[n][k] for the chunk's 32 n; thread xt reads
-        // column k of the raw [32 n][256 k] tile (conflict-free) and writes 8 x 16 bytes
+        // B: row k = bk of the K-major tile holds W[n][k] for the chunk's 32 n; this thread
+        // reads its half of column k of the raw [32 n][256 k] tile (conflict-free) and writes
+        // 4 x 16 bytes of each of the hi and lo rows
         const float* raw = reinterpret_cast<const float*>(smem + kOffRaw + rs * kRawBytes);
         const uint32_t s_bhi = sbase + stage * kStageBytes;
         const uint32_t s_blo = s_bhi + kBTile;
 #pragma unroll
-        for (int ng = 0; ng < 8; ++ng) {
+        for (int g = 0; g < kNgPer; ++g) {
+          const int ng = ng0 + g;
           uint32_t h[4], l[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) split1(raw[(4 * ng + j) * BN + xt], h[j], l[j]);
-          const uint32_t off = xt * 128 + ((ng ^ (xt & 7)) << 4);
+          for (int j = 0; j < 4; ++j) split1(raw[(4 * ng + j) * BN + bk], h[j], l[j]);
+          const uint32_t off = bk * 128 + ((ng ^ (bk & 7)) << 4);
           st_shared_u4(s_bhi + off, h[0], h[1], h[2], h[3]);
           st_shared_u4(s_blo + off, l[0], l[1], l[2], l[3]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_raw_empty(rs));
         if (++rs == kRawStages) rs = 0, rph ^= 1u;
-        // A hi/lo into this stage's TMEM slot, this warp's lane quarter and column half
+        // A hi/lo into this stage's TMEM slot, this warp's lane quarter and 8-column group
         {
-          uint32_t ah[16], al[16];
+          uint32_t ah[kACols], al[kACols];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < kACols / 4; ++j) {
             split1(a4[j].x, ah[4 * j], al[4 * j]);
             split1(a4[j].y, ah[4 * j + 1], al[4 * j + 1]);
             split1(a4[j].z, ah[4 * j + 2], al[4 * j + 2]);
             split1(a4[j].w, ah[4 * j + 3], al[4 * j + 3]);
           }
-          const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 64u * stage + 16u * kh;
-          tmem_st_x16(ta, ah);
-          tmem_st_x16(ta + 32, al);
+          const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 64u * stage + kACols * kh;
+          tmem_st_x8(ta, ah);
+          tmem_st_x8(ta + 32, al);
           tmem_wait_st();
         }
         fence_async_smem();
