@@ -137,3 +137,21 @@ def test_workspace_size_helper(lib):
         assert n == 256 + (4 * slots + 255) // 256 * 256 + slots * 128 * 256 * 4
     else:
         assert n == 0
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_is_self_contained_c_and_cxx(lang, std):
+    """include/mgw.h compiles on its own as strict C99 and as C++17, and every entry point's
+    address can be taken with the declared type (the header is the whole contract)."""
+    import shutil
+    import subprocess
+
+    compiler = "gcc" if lang == "c" else "g++"
+    if shutil.which(compiler) is None:
+        pytest.skip(f"{compiler} not available")
+    uses = "\n".join(f"  (void)&{name};" for name in _declared_functions())
+    src = f'#include "mgw.h"\nint main(void) {{\n{uses}\n  return MGW_OK;\n}}\n'
+    out = subprocess.run([compiler, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-Werror",
+                          "-pedantic", "-fsyntax-only", "-I", os.path.join(ROOT, "include"), "-"],
+                         input=src, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
