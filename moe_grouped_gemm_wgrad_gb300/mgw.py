@@ -4,6 +4,12 @@ Argument marshalling only: every step of the computation runs in the library's
 CUDA kernels.  PyTorch provides device memory and the current stream.  If the
 library is missing or fails to load, every call raises :class:`MgwError`;
 there is no fallback implementation.
+
+The C ABI sees only pointers, so the binding checks what the tensors know and the
+library cannot: dtype, contiguity, one device for all operands, and that every
+caller-supplied buffer holds at least the elements the call reads or writes.  A
+failed check raises :class:`MgwError` before anything is launched.  Each call runs
+with the operands' device current.
 """
 from __future__ import annotations
 
@@ -98,13 +104,67 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev_tensor(t: torch.Tensor, dtype, name: str) -> None:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+def _on_cuda(t: torch.Tensor) -> bool:
+    return t.is_cuda
+
+
+def _dev_tensor(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> None:
+    if not isinstance(t, torch.Tensor) or not _on_cuda(t):
         raise MgwError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise MgwError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise MgwError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise MgwError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+
+
+def _need(t: torch.Tensor, n: int, name: str) -> None:
+    """``t`` holds at least the ``n`` elements the call touches."""
+    if t.numel() < n:
+        raise MgwError(f"{name} holds {t.numel()} elements; the call needs {n}")
+
+
+def _offsets(expert_off: torch.Tensor, E: int | None = None) -> int:
+    """Checks expert_off (int32, E+1 >= 2 entries) and returns E."""
+    _dev_tensor(expert_off, torch.int32, "expert_off", 1)
+    n = expert_off.numel()
+    if n < 2:
+        raise MgwError("expert_off needs E+1 >= 2 entries")
+    if E is not None and n != E + 1:
+        raise MgwError(f"expert_off has {n} entries; {E} experts need {E + 1}")
+    return n - 1
+
+
+def _status(status: torch.Tensor | None) -> None:
+    if status is not None:
+        _dev_tensor(status, torch.int32, "status")
+        _need(status, 1, "status")
+
+
+def _one_device(*ts) -> torch.device:
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) != 1:
+        raise MgwError(f"all tensors must be on one CUDA device, got {sorted(str(d) for d in devs)}")
+    return next(iter(devs))
+
+
+def _out(t: torch.Tensor | None, shape, dtype, dev, name: str) -> torch.Tensor:
+    """The caller's output buffer after checks, or a new one of ``shape``."""
+    n = 1
+    for d in shape:
+        n *= int(d)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=dev)
+    _dev_tensor(t, dtype, name)
+    _need(t, n, name)
+    return t
+
+
+def _device(dev: torch.device):
+    """Makes ``dev`` the current CUDA device for the call (the library launches on, and
+    sizes its grids for, the current device)."""
+    return torch.cuda.device(dev)
 
 
 def token_capacity(M: int, E: int) -> int:
@@ -120,18 +180,17 @@ def mxfp8_quantize(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int | None
                    q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
                    status: torch.Tensor | None = None, stream=None, scale_rule: int = SCALE_FLOOR):
     """MXFP8-quantize bf16 ``src`` [M, C] along tokens -> (q uint8 [C, Mcap], scales uint8)."""
-    _dev_tensor(src, torch.bfloat16, "src")
-    _dev_tensor(expert_off, torch.int32, "expert_off")
+    _dev_tensor(src, torch.bfloat16, "src", 2)
+    E = _offsets(expert_off)
+    _status(status)
     M, C = src.shape
-    E = expert_off.numel() - 1
-    if Mcap is None:
-        Mcap = token_capacity(M, E)
-    if q is None:
-        q = torch.empty((C, Mcap), dtype=torch.uint8, device=src.device)
-    if scales is None:
-        scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
-    st = load().mgw_mxfp8_quantize(_ptr(src), M, C, _ptr(expert_off), E, _ptr(q), _ptr(scales),
-                                   Mcap, int(scale_rule), _ptr(status), _stream(stream))
+    Mcap = token_capacity(M, E) if Mcap is None else int(Mcap)
+    dev = _one_device(src, expert_off, q, scales, status)
+    q = _out(q, (C, Mcap), torch.uint8, dev, "q")
+    scales = _out(scales, (scale_bytes(C, Mcap),), torch.uint8, dev, "scales")
+    with _device(dev):
+        st = load().mgw_mxfp8_quantize(_ptr(src), M, C, _ptr(expert_off), E, _ptr(q), _ptr(scales),
+                                       Mcap, int(scale_rule), _ptr(status), _stream(stream))
     _check(st, "mgw_mxfp8_quantize")
     return q, scales
 
@@ -142,40 +201,52 @@ def mxfp8_quantize_gather(src: torch.Tensor, row_index: torch.Tensor, expert_off
                           stream=None, scale_rule: int = SCALE_FLOOR):
     """MXFP8-quantize the routed rows src[row_index] (src bf16 [rows, C], row_index int32 [M])
     without materialising them -> (q uint8 [C, Mcap], scales uint8)."""
-    _dev_tensor(src, torch.bfloat16, "src")
-    _dev_tensor(row_index, torch.int32, "row_index")
-    _dev_tensor(expert_off, torch.int32, "expert_off")
+    _dev_tensor(src, torch.bfloat16, "src", 2)
+    _dev_tensor(row_index, torch.int32, "row_index", 1)
+    E = _offsets(expert_off)
+    _status(status)
     src_rows, C = src.shape
     M = row_index.numel()
-    E = expert_off.numel() - 1
-    if Mcap is None:
-        Mcap = token_capacity(M, E)
-    if q is None:
-        q = torch.empty((C, Mcap), dtype=torch.uint8, device=src.device)
-    if scales is None:
-        scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
-    st = load().mgw_mxfp8_quantize_gather(_ptr(src), src_rows, _ptr(row_index), M, C,
-                                          _ptr(expert_off), E, _ptr(q), _ptr(scales), Mcap,
-                                          int(scale_rule), _ptr(status), _stream(stream))
+    Mcap = token_capacity(M, E) if Mcap is None else int(Mcap)
+    dev = _one_device(src, row_index, expert_off, q, scales, status)
+    q = _out(q, (C, Mcap), torch.uint8, dev, "q")
+    scales = _out(scales, (scale_bytes(C, Mcap),), torch.uint8, dev, "scales")
+    with _device(dev):
+        st = load().mgw_mxfp8_quantize_gather(_ptr(src), src_rows, _ptr(row_index), M, C,
+                                              _ptr(expert_off), E, _ptr(q), _ptr(scales), Mcap,
+                                              int(scale_rule), _ptr(status), _stream(stream))
     _check(st, "mgw_mxfp8_quantize_gather")
     return q, scales
+
+
+def _wgrad_operands(gq, gs, xq, xs, expert_off, status, *others):
+    """Checks the quantized wgrad operands; returns (E, N, K, Mcap, device)."""
+    for t, n in ((gq, "gq"), (xq, "xq")):
+        _dev_tensor(t, torch.uint8, n, 2)
+    for t, n in ((gs, "gs"), (xs, "xs")):
+        _dev_tensor(t, torch.uint8, n)
+    E = _offsets(expert_off)
+    _status(status)
+    N, Mcap = gq.shape
+    K, Mcap_x = xq.shape
+    if Mcap_x != Mcap:
+        raise MgwError(f"gq [N, {Mcap}] and xq [K, {Mcap_x}] must share one padded token axis")
+    _need(gs, scale_bytes(N, Mcap), "gs")
+    _need(xs, scale_bytes(K, Mcap), "xs")
+    dev = _one_device(gq, gs, xq, xs, expert_off, status, *others)
+    return E, N, K, Mcap, dev
 
 
 def grouped_wgrad_mxfp8(gq: torch.Tensor, gs: torch.Tensor, xq: torch.Tensor, xs: torch.Tensor,
                         expert_off: torch.Tensor, M: int, out: torch.Tensor | None = None,
                         status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """grad_w [E*N, K] bf16 from quantized g^T (N rows) and x^T (K rows)."""
-    for t, n in ((gq, "gq"), (gs, "gs"), (xq, "xq"), (xs, "xs")):
-        _dev_tensor(t, torch.uint8, n)
-    _dev_tensor(expert_off, torch.int32, "expert_off")
-    N, Mcap = gq.shape
-    K = xq.shape[0]
-    E = expert_off.numel() - 1
-    if out is None:
-        out = torch.empty((E * N, K), dtype=torch.bfloat16, device=gq.device)
-    st = load().mgw_grouped_wgrad_mxfp8(_ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off),
-                                        E, int(M), N, K, Mcap, _ptr(out), _ptr(status),
-                                        _stream(stream))
+    E, N, K, Mcap, dev = _wgrad_operands(gq, gs, xq, xs, expert_off, status, out)
+    out = _out(out, (E * N, K), torch.bfloat16, dev, "out")
+    with _device(dev):
+        st = load().mgw_grouped_wgrad_mxfp8(_ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs),
+                                            _ptr(expert_off), E, int(M), N, K, Mcap, _ptr(out),
+                                            _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_wgrad_mxfp8")
     return out
 
@@ -197,17 +268,13 @@ def grouped_wgrad_mxfp8_balanced(gq: torch.Tensor, gs: torch.Tensor, xq: torch.T
     """grad_w [E*N, K] bf16, as :func:`grouped_wgrad_mxfp8`, with split-K and dynamic
     scheduling for skewed routings.  ``workspace``: uint8, zero-filled before first use
     (see :func:`wgrad_workspace`); calls sharing it must not overlap."""
-    for t, n in ((gq, "gq"), (gs, "gs"), (xq, "xq"), (xs, "xs"), (workspace, "workspace")):
-        _dev_tensor(t, torch.uint8, n)
-    _dev_tensor(expert_off, torch.int32, "expert_off")
-    N, Mcap = gq.shape
-    K = xq.shape[0]
-    E = expert_off.numel() - 1
-    if out is None:
-        out = torch.empty((E * N, K), dtype=torch.bfloat16, device=gq.device)
-    st = load().mgw_grouped_wgrad_mxfp8_balanced(
-        _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
-        _ptr(out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _dev_tensor(workspace, torch.uint8, "workspace")
+    E, N, K, Mcap, dev = _wgrad_operands(gq, gs, xq, xs, expert_off, status, out, workspace)
+    out = _out(out, (E * N, K), torch.bfloat16, dev, "out")
+    with _device(dev):
+        st = load().mgw_grouped_wgrad_mxfp8_balanced(
+            _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
+            _ptr(out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_wgrad_mxfp8_balanced")
     return out
 
@@ -219,17 +286,12 @@ def grouped_wgrad_mxfp8_balanced_noalloc(gq: torch.Tensor, gs: torch.Tensor, xq:
                                          stream=None) -> torch.Tensor:
     """As :func:`grouped_wgrad_mxfp8_balanced` on the library's own workspace (a device array
     in the library; nothing is allocated, calls must not overlap)."""
-    for t, n in ((gq, "gq"), (gs, "gs"), (xq, "xq"), (xs, "xs")):
-        _dev_tensor(t, torch.uint8, n)
-    _dev_tensor(expert_off, torch.int32, "expert_off")
-    N, Mcap = gq.shape
-    K = xq.shape[0]
-    E = expert_off.numel() - 1
-    if out is None:
-        out = torch.empty((E * N, K), dtype=torch.bfloat16, device=gq.device)
-    st = load().mgw_grouped_wgrad_mxfp8_balanced_noalloc(
-        _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
-        _ptr(out), _ptr(status), _stream(stream))
+    E, N, K, Mcap, dev = _wgrad_operands(gq, gs, xq, xs, expert_off, status, out)
+    out = _out(out, (E * N, K), torch.bfloat16, dev, "out")
+    with _device(dev):
+        st = load().mgw_grouped_wgrad_mxfp8_balanced_noalloc(
+            _ptr(gq), _ptr(gs), _ptr(xq), _ptr(xs), _ptr(expert_off), E, int(M), N, K, Mcap,
+            _ptr(out), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_wgrad_mxfp8_balanced_noalloc")
     return out
 
@@ -238,15 +300,19 @@ def grouped_dgrad_f32(dy: torch.Tensor, W: torch.Tensor, expert_off: torch.Tenso
                       out: torch.Tensor | None = None, status: torch.Tensor | None = None,
                       stream=None) -> torch.Tensor:
     """dx [rows, in_f] fp32 = dy[r] . W[e(r)] per row's expert."""
-    _dev_tensor(dy, torch.float32, "dy")
-    _dev_tensor(W, torch.float32, "W")
-    _dev_tensor(expert_off, torch.int32, "expert_off")
+    _dev_tensor(dy, torch.float32, "dy", 2)
+    _dev_tensor(W, torch.float32, "W", 3)
     rows, out_f = dy.shape
-    E, _, in_f = W.shape
-    if out is None:
-        out = torch.empty((rows, in_f), dtype=torch.float32, device=dy.device)
-    st = load().mgw_grouped_dgrad_f32(_ptr(dy), _ptr(W), _ptr(expert_off), E, rows, out_f, in_f,
-                                      _ptr(out), _ptr(status), _stream(stream))
+    E, out_w, in_f = W.shape
+    if out_w != out_f:
+        raise MgwError(f"W [E, {out_w}, in_f] does not match dy [rows, {out_f}]")
+    _offsets(expert_off, E)
+    _status(status)
+    dev = _one_device(dy, W, expert_off, out, status)
+    out = _out(out, (rows, in_f), torch.float32, dev, "out")
+    with _device(dev):
+        st = load().mgw_grouped_dgrad_f32(_ptr(dy), _ptr(W), _ptr(expert_off), E, rows, out_f,
+                                          in_f, _ptr(out), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_dgrad_f32")
     return out
 
@@ -258,24 +324,23 @@ def mxfp8_quantize_rows(src: torch.Tensor, expert_off: torch.Tensor, Mcap: int |
     """Row-wise MXFP8 quantization (one scale per 32 columns of a row) of the routed rows:
     ``src[row_index]`` when ``row_index`` (int32 [M]) is given, else ``src`` [M, C].
     -> (q uint8 [Mcap, C] on the padded row axis, scale atoms uint8)."""
-    _dev_tensor(src, torch.bfloat16, "src")
-    _dev_tensor(expert_off, torch.int32, "expert_off")
+    _dev_tensor(src, torch.bfloat16, "src", 2)
+    E = _offsets(expert_off)
+    _status(status)
     src_rows, C = src.shape
     if row_index is not None:
-        _dev_tensor(row_index, torch.int32, "row_index")
+        _dev_tensor(row_index, torch.int32, "row_index", 1)
         M = row_index.numel()
     else:
         M = src_rows
-    E = expert_off.numel() - 1
-    if Mcap is None:
-        Mcap = token_capacity(M, E)
-    if q is None:
-        q = torch.empty((Mcap, C), dtype=torch.uint8, device=src.device)
-    if scales is None:
-        scales = torch.empty((scale_bytes(C, Mcap),), dtype=torch.uint8, device=src.device)
-    st = load().mgw_mxfp8_quantize_rows(_ptr(src), src_rows, _ptr(row_index), M, C,
-                                        _ptr(expert_off), E, _ptr(q), _ptr(scales), Mcap,
-                                        int(scale_rule), _ptr(status), _stream(stream))
+    Mcap = token_capacity(M, E) if Mcap is None else int(Mcap)
+    dev = _one_device(src, expert_off, row_index, q, scales, status)
+    q = _out(q, (Mcap, C), torch.uint8, dev, "q")
+    scales = _out(scales, (scale_bytes(C, Mcap),), torch.uint8, dev, "scales")
+    with _device(dev):
+        st = load().mgw_mxfp8_quantize_rows(_ptr(src), src_rows, _ptr(row_index), M, C,
+                                            _ptr(expert_off), E, _ptr(q), _ptr(scales), Mcap,
+                                            int(scale_rule), _ptr(status), _stream(stream))
     _check(st, "mgw_mxfp8_quantize_rows")
     return q, scales
 
@@ -285,17 +350,24 @@ def grouped_fprop_mxfp8(xq: torch.Tensor, xs: torch.Tensor, wq: torch.Tensor, ws
                         status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y [M, N] bf16 = x[r] . W[e(r)]^T from row-wise quantized x [Mcap, K] and W [Mw, K]
     (W [E, N, K] quantized with offsets {0, N, ..., E*N})."""
-    for t, n in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
+    for t, n in ((xq, "xq"), (wq, "wq")):
+        _dev_tensor(t, torch.uint8, n, 2)
+    for t, n in ((xs, "xs"), (ws, "ws")):
         _dev_tensor(t, torch.uint8, n)
-    _dev_tensor(expert_off, torch.int32, "expert_off")
+    E = _offsets(expert_off)
+    _status(status)
     Mcap, K = xq.shape
-    Mw = wq.shape[0]
-    E = expert_off.numel() - 1
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
-    st = load().mgw_grouped_fprop_mxfp8(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(expert_off),
-                                        E, int(M), int(N), K, Mcap, Mw, _ptr(out), _ptr(status),
-                                        _stream(stream))
+    Mw, K_w = wq.shape
+    if K_w != K:
+        raise MgwError(f"wq [Mw, {K_w}] and xq [Mcap, {K}] must share the contraction width")
+    _need(xs, scale_bytes(K, Mcap), "xs")
+    _need(ws, scale_bytes(K, Mw), "ws")
+    dev = _one_device(xq, xs, wq, ws, expert_off, out, status)
+    out = _out(out, (int(M), int(N)), torch.bfloat16, dev, "out")
+    with _device(dev):
+        st = load().mgw_grouped_fprop_mxfp8(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws),
+                                            _ptr(expert_off), E, int(M), int(N), K, Mcap, Mw,
+                                            _ptr(out), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_fprop_mxfp8")
     return out
 
@@ -306,16 +378,21 @@ def grouped_dgrad_mxfp8(dyq: torch.Tensor, dys: torch.Tensor, wtq: torch.Tensor,
                         stream=None) -> torch.Tensor:
     """dx [M, K] bf16 = dy[r] . W[e(r)] from row-wise quantized dy [Mcap, N] and W quantized
     along n per expert by :func:`mxfp8_quantize` (wtq [K, Mw])."""
-    for t, n in ((dyq, "dyq"), (dys, "dys"), (wtq, "wtq"), (wts, "wts")):
+    for t, n in ((dyq, "dyq"), (wtq, "wtq")):
+        _dev_tensor(t, torch.uint8, n, 2)
+    for t, n in ((dys, "dys"), (wts, "wts")):
         _dev_tensor(t, torch.uint8, n)
-    _dev_tensor(expert_off, torch.int32, "expert_off")
+    E = _offsets(expert_off)
+    _status(status)
     Mcap, N = dyq.shape
     K, Mw = wtq.shape
-    E = expert_off.numel() - 1
-    if out is None:
-        out = torch.empty((M, K), dtype=torch.bfloat16, device=dyq.device)
-    st = load().mgw_grouped_dgrad_mxfp8(_ptr(dyq), _ptr(dys), _ptr(wtq), _ptr(wts),
-                                        _ptr(expert_off), E, int(M), N, K, Mcap, Mw, _ptr(out),
-                                        _ptr(status), _stream(stream))
+    _need(dys, scale_bytes(N, Mcap), "dys")
+    _need(wts, scale_bytes(K, Mw), "wts")
+    dev = _one_device(dyq, dys, wtq, wts, expert_off, out, status)
+    out = _out(out, (int(M), K), torch.bfloat16, dev, "out")
+    with _device(dev):
+        st = load().mgw_grouped_dgrad_mxfp8(_ptr(dyq), _ptr(dys), _ptr(wtq), _ptr(wts),
+                                            _ptr(expert_off), E, int(M), N, K, Mcap, Mw,
+                                            _ptr(out), _ptr(status), _stream(stream))
     _check(st, "mgw_grouped_dgrad_mxfp8")
     return out
