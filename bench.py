@@ -69,21 +69,33 @@ class ClockSampler:
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int, path: str | None):
+    def __init__(self, gpu_index: int, path: str | None = None, cmd: list | None = None,
+                 settle_s: float = 1.0):
+        """Starts sampling GPU ``gpu_index``; the raw lines also go to ``path`` if given.
+        ``cmd`` replaces the nvidia-smi command line (same CSV columns)."""
+        import threading
+
         self.proc = None
         self.path = path
         self.window = None
-        if path is None:
-            return
+        self.lines = []
         try:
-            self.fh = open(path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(1.0)  # let the sampler come up before the timed region
+            if cmd is None:
+                cmd = ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
+                       "--format=csv,noheader,nounits", "-lms", "50"]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
         except Exception:
             self.proc = None
+            return
+        # drain the pipe continuously so that nvidia-smi never blocks on a full pipe
+        self.reader = threading.Thread(target=self._drain, daemon=True)
+        self.reader.start()
+        time.sleep(settle_s)  # let the sampler come up before the timed region
+
+    def _drain(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
 
     def mark(self, t0: float, t1: float):
         self.window = (t0, t1)
@@ -97,20 +109,22 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        self.fh.close()
+        self.reader.join(timeout=5)
+        if self.path is not None:
+            with open(self.path, "w") as f:
+                f.writelines(self.lines)
         import datetime
 
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                try:
-                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
-                except ValueError:
-                    continue
+        for line in list(self.lines):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
+            except ValueError:
+                continue
         inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
         use = inside if inside else rows
         if not use:
@@ -138,7 +152,7 @@ def dgrad_case(name):
     return getattr(synth, name)()
 
 
-def run_wgrad(name, steps, warmup, dist_ctx):
+def run_wgrad(name, steps, warmup, dist_ctx, clocks_csv=None):
     import torch
 
     from moe_grouped_gemm_wgrad_gb300 import mgw
@@ -178,8 +192,9 @@ def run_wgrad(name, steps, warmup, dist_ctx):
         quant_x()
         mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
 
-    clocks = ClockSampler(dist_ctx.local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_r{dist_ctx.rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    # raw clock samples go to a CSV only when asked for (one file per rank)
+    csv_path = None if clocks_csv is None else f"{clocks_csv}.r{dist_ctx.rank}" if dist_ctx.world > 1 else clocks_csv
+    clocks = ClockSampler(dist_ctx.local_rank, csv_path)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -536,6 +551,8 @@ def main():
     ap.add_argument("--skew-workload", default="wgrad_skew",
                     choices=["wgrad_skew", "wgrad_8192", "moe_ffn_pair", "none"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also write the raw nvidia-smi clock samples of the timed step to this CSV")
     args = ap.parse_args()
     peaks = _peaks()
     # nominal fp8 : bf16 dense ratio 4.5 : 2.25; the sustained figure applies to a kernel
@@ -580,7 +597,7 @@ def main():
     from moe_grouped_gemm_wgrad_gb300 import build as _build
 
     _build.build()  # no-op when current
-    r = run_wgrad(args.workload, args.steps, args.warmup, d)
+    r = run_wgrad(args.workload, args.steps, args.warmup, d, args.clocks_csv)
     dg = None
     if args.dgrad_workload != "none":
         dg = run_dgrad(args.dgrad_workload, max(5, min(args.steps, 50)), max(3, args.warmup))

@@ -55,3 +55,50 @@ def test_cpu_baseline_sizes_its_sample_from_a_pilot():
     side = int(cb["sample"].split("grad_w block ")[1].split("x")[0])
     assert side % 128 == 0 and 128 <= side <= 1024
     assert "1024 tokens" in cb["sample"]
+
+
+def test_clock_sampler_summarises_the_timed_window_without_a_csv():
+    """The clock record needs no output folder: samples come through a drained pipe, only
+    those inside the marked window are summarised, and active throttle reasons are named."""
+    import datetime
+    import time
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    now = time.time()
+    fmt = "%Y/%m/%d %H:%M:%S.%f"
+
+    def line(t, mhz, cap):
+        ts = datetime.datetime.fromtimestamp(t).strftime(fmt)[:-3]
+        return f"{ts}, 0, {mhz}, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, {cap}"
+
+    lines = [line(now - 50, 1000, "Not Active")]                    # before the window
+    lines += [line(now - 5 + 0.1 * i, 1950 + i, "Active") for i in range(5)]
+    lines += [line(now + 50, 500, "Not Active")]                    # after the window
+    # many more lines than a pipe buffer holds, then wait to be terminated
+    script = ("import sys, time\n"
+              f"lines = {lines!r}\n"
+              "filler = 'x' * 200\n"
+              "for i in range(2000): print(filler)\n"
+              "for l in lines: print(l)\n"
+              "sys.stdout.flush()\n"
+              "time.sleep(60)\n")
+    sampler = bench.ClockSampler(0, cmd=[sys.executable, "-c", script], settle_s=0.0)
+    deadline = time.time() + 30
+    while len(sampler.lines) < 2000 + len(lines) and time.time() < deadline:
+        time.sleep(0.05)
+    sampler.mark(now - 10, now + 10)
+    clk = sampler.stop()
+    assert clk is not None
+    assert clk["samples_in_timed_window"] == 5 and clk["samples"] == 5
+    assert clk["sm_mhz"] == 1952.0 and clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi_reports_nothing():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    sampler = bench.ClockSampler(0, cmd=["/nonexistent/nvidia-smi"], settle_s=0.0)
+    assert sampler.stop() is None
