@@ -11,6 +11,11 @@
  * caller's int status word, and the kernels then leave their outputs untouched.
  * No entry point aborts, traps or blocks the host.
  *
+ * Limits common to every entry point: device pointers 16-byte aligned (else
+ * MGW_ERR_INVALID_ARG); a padded token or row axis Mcap (or Mw) of at most 2^31
+ * (else MGW_ERR_CAPACITY); 1 <= E <= MGW_MAX_EXPERTS.  The current device must be
+ * compute capability 10.3 (else MGW_ERR_ARCH).
+ *
  * Pages restated (cited by title and part):
  *   wgrad page  "tinygrad/extra/thunder/amd/grouped_mxfp8_wgrad.cpp" -- the
  *               grouped MXFP8 expert weight gradient kernel.
@@ -144,6 +149,8 @@ mgw_status mgw_mxfp8_quantize_gather(const void *src_bf16, int src_rows,
  * expert_off device int32 [E+1], as for the quantizer; M = expert_off[E].
  * N          grad_w rows per expert, a positive multiple of 128.
  * K          grad_w columns, a positive multiple of 256.
+ *            E*N <= 2^31 and E * (N/128) * (K/256) < 2^31 (output rows and tiles are
+ *            counted in 32 bits); else MGW_ERR_UNSUPPORTED.
  * Mcap       the padded token axis both operands were quantized on.
  * out_bf16   device, bf16 [E*N, K] row-major, fully written.
  * status_dev device int, nullable (see MGW_DEV_*).
