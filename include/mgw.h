@@ -275,6 +275,7 @@ mgw_status mgw_mxfp8_quantize_rows(const void *src_bf16, int src_rows, const int
  *          [E*N, K] with offsets {0, N, 2N, ..., E*N} (W[e][n] is row e*N + n):
  *          [Mw, K] with Mw its Mcap.
  * N a positive multiple of 256; K a positive multiple of 128.
+ * Mw a multiple of 128 and >= E*N (else MGW_ERR_CAPACITY).
  * y_bf16   device, bf16 [M, N] row-major, fully written (round to nearest even).
  * Accumulation is fp32 in tensor memory; no bound beyond fp32 summation error. */
 mgw_status mgw_grouped_fprop_mxfp8(const void *xq, const void *xs, const void *wq,
@@ -290,6 +291,7 @@ mgw_status mgw_grouped_fprop_mxfp8(const void *xq, const void *xs, const void *w
  *          tokens-by-features with offsets {0, N, ..., E*N}: [K, Mw] with Mw its Mcap,
  *          W[e][n][k] at row k, column e*N + n.
  * N a positive multiple of 128; K a positive multiple of 256.
+ * Mw a multiple of 128 and >= E*N (else MGW_ERR_CAPACITY).
  * dx_bf16  device, bf16 [M, K] row-major, fully written. */
 mgw_status mgw_grouped_dgrad_mxfp8(const void *dyq, const void *dys, const void *wtq,
                                    const void *wts, const int32_t *expert_off, int E, int M,
