@@ -96,8 +96,22 @@ def test_argument_errors_forward_and_mx_dgrad(lib):
     assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 64, 256, 256, 256, fake, None, None) == -2
     assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, fake, fake, fake, 1, 4, 128, 128, 256, 256, fake, None, None) == -2
     assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, P(0x1004), fake, fake, 1, 4, 128, 256, 256, 256, fake, None, None) == -1
+    # Mw below E*N, or not a multiple of 128
+    assert lib.mgw_grouped_dgrad_mxfp8(fake, fake, fake, fake, fake, 2, 4, 128, 256, 384, 128, fake, None, None) == -3
+    assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 1, 4, 256, 128, 256, 320, fake, None, None) == -3
     # no rows: the output may be null only then
     assert lib.mgw_grouped_fprop_mxfp8(fake, fake, fake, fake, fake, 1, 4, 256, 128, 256, 256, None, None, None) == -1
+
+
+def test_wgrad_32bit_size_limits(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # E*N above 2^31 output rows
+    assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1024, 4, (1 << 21) + 128, 256,
+                                       1 << 17, fake, None, None) == -2
+    # E*N = 2^31 is allowed, but 1024 x 16384 x 128 = 2^31 output tiles is not
+    assert lib.mgw_grouped_wgrad_mxfp8(fake, fake, fake, fake, fake, 1024, 4, 1 << 21, 1 << 15,
+                                       1 << 17, fake, None, None) == -2
 
 
 def test_argument_errors_balanced_wgrad(lib):
