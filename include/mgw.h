@@ -4,11 +4,13 @@
  * C ABI of libmgw.so.  Every entry point takes plain device pointers, sizes and
  * a CUDA stream handle; nothing here depends on PyTorch.  All device work is
  * asynchronous on `stream` (a cudaStream_t passed as void*; NULL means the
- * legacy default stream).  The library allocates no device memory: the caller
- * owns every buffer.  Host-detectable argument errors return a negative status
- * before anything is launched; data errors that only the device can see (an
- * invalid expert_off array) are reported by OR-ing MGW_DEV_* bits into the
- * caller's int status word, and the kernels then leave their outputs untouched.
+ * legacy default stream).  No entry point calls an allocator: the caller owns
+ * every buffer it passes, and the one library-owned buffer is the static device
+ * workspace of mgw_grouped_wgrad_mxfp8_balanced_noalloc.  Host-detectable
+ * argument errors return a negative status before anything is launched; data
+ * errors that only the device can see (an invalid expert_off array) are reported
+ * by OR-ing MGW_DEV_* bits into the caller's int status word, and the kernels
+ * then leave their outputs untouched.
  * No entry point aborts, traps or blocks the host.
  *
  * Limits common to every entry point: device pointers 16-byte aligned (else
@@ -192,13 +194,29 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void *gq, const void *gs, cons
                                             void *workspace, size_t workspace_bytes,
                                             int *status_dev, void *stream);
 
-/* mgw_grouped_wgrad_mxfp8_balanced_noalloc -- mgw_grouped_wgrad_mxfp8_balanced on a
- * workspace the library owns: a 16 MB device array (room for 128 partial tiles) defined in
- * the library and zero-filled when it loads, one per device.  The call allocates no memory
- * and takes no workspace argument.  Because every call on a device shares that array,
- * calls on different streams must not run concurrently; after MGW_DEV_TIMEOUT the array's
- * counters are undefined and the process must not use this entry point again.  Arguments,
- * result and errors otherwise as mgw_grouped_wgrad_mxfp8_balanced. */
+/* mgw_grouped_wgrad_mxfp8_balanced_noalloc -- mgw_grouped_wgrad_mxfp8_balanced for callers
+ * that cannot allocate device memory: code running inside a memory pool or an allocator
+ * that must not be re-entered, a captured graph's fixed memory plan, or an embedding that
+ * owns every allocation of the process.  The pages have no counterpart to this entry point;
+ * it exists for those callers only.
+ *
+ * The workspace is owned by the library: a 16 MB device array (the counters plus room for
+ * 128 fp32 partial tiles of 128 x 256) defined in the library, zero-filled when the library
+ * loads, held by every GPU that loads it until the process exits.  The call allocates and
+ * frees nothing (no cudaMalloc, no cudaFree, no allocating library routine).  Its device
+ * address is looked up with cudaGetSymbolAddress on the first call in each CUDA context
+ * (again after the context is re-created), so make that first call before any stream
+ * capture.  Every call first clears the array's counters (under 1 KB, cudaMemsetAsync on
+ * `stream`), so a call after one that ended with MGW_DEV_TIMEOUT starts clean.  Every call
+ * on a device shares the one array: calls whose work overlaps on the GPU (different
+ * streams, or several host threads) race and give undefined results.
+ *
+ * The 128 partial slots bound the split-K: splits apply only while the split tiles'
+ * partials, sum over split experts of (N/128)*(K/256)*S, fit in 128; otherwise the target
+ * item length doubles until they do, and with more than 64 output tiles per expert no
+ * expert is split (every call still gets the longest-first dynamic scheduling).  No size
+ * is rejected for the workspace's sake.  Arguments, result, limits (E <= 512) and errors
+ * otherwise as mgw_grouped_wgrad_mxfp8_balanced. */
 mgw_status mgw_grouped_wgrad_mxfp8_balanced_noalloc(const void *gq, const void *gs,
                                                     const void *xq, const void *xs,
                                                     const int32_t *expert_off, int E, int M,

@@ -16,6 +16,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmgw.so")
+# Test build: the same objects, except the C ABI compiled with MGW_TEST_HOOKS, which lets
+# the device time-limit test make a pipeline stage that never fills (MGW_TEST_DROP_LOAD=1).
+# libmgw.so itself has no such switch.
+LIB_TESTHOOKS = os.path.join(HERE, "libmgw_testhooks.so")
 SOURCES = ["api.cu", "quantize.cu", "quantize_rows.cu", "wgrad.cu", "wgrad_balanced.cu", "wgrad_noalloc.cu", "grouped_mm.cu", "dgrad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -36,29 +40,40 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc()] + NVCC_FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(job: tuple[str, tuple[str, ...]]) -> tuple[str, str]:
+    src, defines = job
+    stem = os.path.splitext(src)[0] + ("_hooks" if defines else "")
+    obj = os.path.join(BUILD, stem + ".o")
+    cmd = [nvcc()] + NVCC_FLAGS + list(defines) + ["-c", os.path.join(CSRC, src), "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{res.stdout}\n{res.stderr}")
     return obj, res.stderr
 
 
+def _link(out: str, objs: list[str]) -> None:
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs)
+    os.replace(tmp, out)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libmgw.so if any source is newer than it; returns its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    """Compile libmgw.so (and its test build) if any source is newer; returns its path."""
+    newest = _deps_mtime()
+    if (not force and all(os.path.exists(p) and os.path.getmtime(p) >= newest
+                          for p in (LIB, LIB_TESTHOOKS))):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(_compile, SOURCES))
+    jobs = [(src, ()) for src in SOURCES] + [("api.cu", ("-DMGW_TEST_HOOKS",))]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(_compile, jobs))
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
+    objs = [o for o, _ in results[:len(SOURCES)]]
+    _link(LIB, objs)
+    hooks = [results[-1][0] if os.path.basename(o) == "api.o" else o for o in objs]
+    _link(LIB_TESTHOOKS, hooks)
     return LIB
 
 

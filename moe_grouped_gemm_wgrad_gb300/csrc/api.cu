@@ -60,10 +60,45 @@ mgw_status current_device(DeviceInfo* info) {
 }
 
 // 2-D tiled tensor map: `inner` contiguous elements per row, `outer` rows,
-// `pitch` bytes between rows.
+// `pitch` bytes between rows.  A tensor map is plain data (base address, sizes, strides,
+// box and swizzle), so encoded maps are kept in a small process-wide table keyed by every
+// one of those inputs and reused by later calls on the same buffers.
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer, pitch;
+  uint32_t box_inner, box_outer;
+  int dt, swz;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && pitch == o.pitch &&
+           box_inner == o.box_inner && box_outer == o.box_outer && dt == o.dt && swz == o.swz;
+  }
+};
+constexpr int kMapCacheSize = 64;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCacheSize];
+  CUtensorMap map[kMapCacheSize];
+  int used = 0, next = 0;
+};
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                  uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swz) {
+  const MapKey k{base, inner, outer, pitch, box_inner, box_outer, static_cast<int>(dt),
+                 static_cast<int>(swz)};
+  MapCache& c = map_cache();
+  {
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (int i = 0; i < c.used; ++i)
+      if (c.key[i] == k) {
+        *m = c.map[i];
+        return true;
+      }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -71,14 +106,62 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   std::memset(m, 0, sizeof(*m));
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(c.mu);
+  const int slot = c.used < kMapCacheSize ? c.used++ : (c.next++ % kMapCacheSize);
+  c.key[slot] = k;
+  c.map[slot] = *m;
+  return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+namespace mgw {
+
+uint64_t current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return static_cast<uint64_t>(id);
+}
+
+cudaError_t set_smem_attr_once(const void* kernel, size_t bytes, uint64_t* done_ctx) {
+  const uint64_t id = current_context_id();
+  if (id != 0 && id == *done_ctx) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(bytes));
+  if (err != cudaSuccess) return err;
+  // The call above made the device's context current if no context was.
+  *done_ctx = current_context_id();
+  return cudaSuccess;
+}
+
+}  // namespace mgw
 
 extern "C" {
 
@@ -189,22 +272,15 @@ mgw_status wgrad_check(const void* gq, const void* gs, const void* xq, const voi
   return MGW_OK;
 }
 
-// Tensor maps and sizes of the wgrad kernels; box_b is the x^T box height (256, or 128 for
-// CTA pairs).
+// Tensor maps and sizes of the wgrad kernels.
 bool wgrad_maps(mgw::WgradArgs* a, const void* gq, const void* gs, const void* xq,
                 const void* xs, const int32_t* expert_off, int E, int M, int N, int K,
-                size_t Mcap, void* out_bf16, int* status_dev, uint32_t box_b) {
+                size_t Mcap, void* out_bf16, int* status_dev) {
   std::memset(a, 0, sizeof(*a));
   if (!make_map_2d(&a->tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, Mcap, N, Mcap, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&a->tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128, box_b,
+      !make_map_2d(&a->tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128, 256,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&a->tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, 256,
-                   static_cast<uint64_t>(N) * (Mcap / 32) / 256, 256, 256, 2,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&a->tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, 256,
-                   static_cast<uint64_t>(K) * (Mcap / 32) / 256, 256, 256, 4,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(&a->tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_bf16, K,
                    static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))
@@ -249,7 +325,7 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void* gq, const void* gs, cons
   st = current_device(&dev);
   if (st != MGW_OK) return st;
   mgw::WgradArgs a;
-  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev, 256))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev))
     return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_grouped_wgrad_balanced(a, workspace, slots, dev.sms,
                                                              static_cast<cudaStream_t>(stream));
@@ -268,11 +344,16 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced_noalloc(const void* gq, const void* 
   st = current_device(&dev);
   if (st != MGW_OK) return st;
   void* ws = nullptr;
-  size_t ws_bytes = 0;
-  if (mgw::noalloc_wgrad_workspace(&ws, &ws_bytes) != cudaSuccess) return MGW_ERR_CUDA;
+  size_t ws_bytes = 0, counter_bytes = 0;
+  if (mgw::noalloc_wgrad_workspace(&ws, &ws_bytes, &counter_bytes) != cudaSuccess)
+    return MGW_ERR_CUDA;
   const int slots = mgw::balanced_workspace_slots(ws_bytes);
+  // The kernel leaves its counters at zero, but a call that ended with MGW_DEV_TIMEOUT may
+  // not have: clear them (under 1 KB, on the call's stream) so every call starts clean.
+  if (cudaMemsetAsync(ws, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MGW_ERR_CUDA;
   mgw::WgradArgs a;
-  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev, 256))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev))
     return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_grouped_wgrad_balanced(a, ws, slots, dev.sms,
                                                              static_cast<cudaStream_t>(stream));
@@ -289,13 +370,15 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* x
   mgw_status st = current_device(&dev);
   if (st != MGW_OK) return st;
   mgw::WgradArgs a;
-  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev,
-                  mgw::wgrad_uses_pair(N) ? 128 : 256))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev))
     return MGW_ERR_CUDA;
+#ifdef MGW_TEST_HOOKS
   {
-    const char* v = std::getenv("MGW_TEST_DROP_LOAD");  // test hook, see kernels.h
+    // Only in the test build of the library (libmgw_testhooks.so), see kernels.h.
+    const char* v = std::getenv("MGW_TEST_DROP_LOAD");
     a.drop_first_load = (v != nullptr && v[0] == '1') ? 1 : 0;
   }
+#endif
   const cudaError_t err = mgw::launch_grouped_wgrad(a, dev.sms, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }

@@ -391,16 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
 }  // namespace
 
 cudaError_t launch_grouped_dgrad(const DgradArgs& a, int num_sms, cudaStream_t stream) {
-  static thread_local int attr_set_device = -1;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static thread_local uint64_t attr_ctx = 0;
+  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(grouped_dgrad_kernel),
+                                       dgrad_smem_bytes(kMaxExperts), &attr_ctx);
   if (err != cudaSuccess) return err;
-  if (attr_set_device != dev) {
-    err = cudaFuncSetAttribute(grouped_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(dgrad_smem_bytes(kMaxExperts)));
-    if (err != cudaSuccess) return err;
-    attr_set_device = dev;
-  }
   // Upper bound of the item count without reading expert_off on the host:
   // sum_e ceil(cnt_e/128) <= rows/128 + E.
   const long long max_items = (static_cast<long long>(a.rows) / BM + a.E) * (a.in_f / BN);

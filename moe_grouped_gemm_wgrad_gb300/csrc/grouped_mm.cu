@@ -345,16 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mm_mxfp8_kernel(const __g
 }  // namespace
 
 cudaError_t launch_grouped_mm_mxfp8(const MmArgs& a, int num_sms, cudaStream_t stream) {
-  static thread_local int attr_set_device = -1;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static thread_local uint64_t attr_ctx = 0;
+  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(grouped_mm_mxfp8_kernel),
+                                       mm_smem_bytes(kMaxExperts), &attr_ctx);
   if (err != cudaSuccess) return err;
-  if (attr_set_device != dev) {
-    err = cudaFuncSetAttribute(grouped_mm_mxfp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(mm_smem_bytes(kMaxExperts)));
-    if (err != cudaSuccess) return err;
-    attr_set_device = dev;
-  }
   // Upper bound on the used row tiles (the exact count is known on the device only).
   const long long max_tiles = a.Mcap / BM;
   const long long total = max_tiles * (a.J / BN);

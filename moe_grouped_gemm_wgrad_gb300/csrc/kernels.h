@@ -21,15 +21,18 @@ cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& 
                                   cudaStream_t stream, const void* gsrc = nullptr,
                                   const int32_t* row_index = nullptr, int src_rows = 0);
 
-// True when grad_w tiles go to CTA pairs (tcgen05 cta_group::2); this sets the box
-// height of tm_b (128 rows for pairs, 256 otherwise) and whether tm_sfa/tm_sfb are used.
-bool wgrad_uses_pair(int N);
+// Unique id of the calling thread's current CUDA context, or 0 when there is none yet.
+// Unlike a context handle it is never reused within the process, so per-context state
+// (kernel attributes, module symbol addresses) keyed on it is set up again for a context
+// that was destroyed and re-created (cudaDeviceReset).
+uint64_t current_context_id();
+
+// Sets the kernel's maximum dynamic shared memory once per context and calling thread.
+cudaError_t set_smem_attr_once(const void* kernel, size_t bytes, uint64_t* done_ctx);
 
 struct WgradArgs {
   CUtensorMap tm_a;    // g^T e4m3 [N, Mcap], box 128 tokens x 128 rows, 128B swizzle
-  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x (128 or 256) rows, 128B swizzle
-  CUtensorMap tm_sfa;  // g scale atoms as 256-byte rows, box 256 x 2 (one atom)
-  CUtensorMap tm_sfb;  // x scale atoms as 256-byte rows, box 256 x 4 (two atoms)
+  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x 256 rows, 128B swizzle
   CUtensorMap tm_out;  // grad_w bf16 [E*N, K], box 64 cols x 128 rows, 128B swizzle
   void* out;           // grad_w (plain stores of the zero tiles)
   const uint8_t* gs;   // g scale atoms
@@ -37,9 +40,10 @@ struct WgradArgs {
   const int32_t* expert_off;
   int E, M, N, K;
   int* status;
-  // Test hook for the device time limit: when set, the single-SM kernel's producer
-  // announces its first chunk's bytes but never issues the copies, so the waits on that
-  // stage run out and the kernel reports MGW_DEV_TIMEOUT.  Zero in normal use.
+  // Test hook for the device time limit: when set, the static kernel's producer announces
+  // its first chunk's bytes but never issues the copies, so the waits on that stage run out
+  // and the kernel reports MGW_DEV_TIMEOUT.  Always zero in libmgw.so; only the test build
+  // libmgw_testhooks.so (compiled with MGW_TEST_HOOKS) sets it, from MGW_TEST_DROP_LOAD=1.
   int drop_first_load;
   // Load-balanced kernel only (wgrad_balanced.cu): the workspace.
   int* ws_sched;   // [0] next item, [1] CTAs finished (zero at rest)
@@ -59,8 +63,10 @@ int balanced_workspace_slots(size_t bytes);   // -1 when smaller than the header
 size_t balanced_workspace_bytes(int slots);
 cudaError_t launch_grouped_wgrad_balanced(WgradArgs a, void* workspace, int slots, int num_sms,
                                           cudaStream_t stream);
-// The library-owned workspace of the no-allocation entry point (wgrad_noalloc.cu).
-cudaError_t noalloc_wgrad_workspace(void** ptr, size_t* bytes);
+// The library-owned workspace of the no-allocation entry point (wgrad_noalloc.cu): its
+// device address in the current context, its size, and the size of its leading counter
+// region (header and tile counters), which each call clears before it launches.
+cudaError_t noalloc_wgrad_workspace(void** ptr, size_t* bytes, size_t* counter_bytes);
 
 // Row-wise MXFP8 quantization (quantize_rows.cu): routed row r (source row row_index[r],
 // or r when row_index is null) of expert e goes to padded row P[e] + r - off[e] of

@@ -279,18 +279,13 @@ cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& 
                                   cudaStream_t stream, const void* gsrc,
                                   const int32_t* row_index, int src_rows) {
   const size_t smem = quantize_smem_bytes(E);
-  static thread_local int attr_set_device = -1;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static thread_local uint64_t attr_ctx[2] = {0, 0};
+  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mxfp8_quantize_kernel<false>),
+                                       quantize_smem_bytes(kMaxExperts), &attr_ctx[0]);
   if (err != cudaSuccess) return err;
-  if (attr_set_device != dev) {
-    for (auto fn : {mxfp8_quantize_kernel<false>, mxfp8_quantize_kernel<true>}) {
-      err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(quantize_smem_bytes(kMaxExperts)));
-      if (err != cudaSuccess) return err;
-    }
-    attr_set_device = dev;
-  }
+  err = set_smem_attr_once(reinterpret_cast<const void*>(mxfp8_quantize_kernel<true>),
+                           quantize_smem_bytes(kMaxExperts), &attr_ctx[1]);
+  if (err != cudaSuccess) return err;
   const bool gather = row_index != nullptr;
   auto kernel = gather ? mxfp8_quantize_kernel<true> : mxfp8_quantize_kernel<false>;
   int per_sm = 0;

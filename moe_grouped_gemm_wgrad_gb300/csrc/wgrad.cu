@@ -379,340 +379,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
 }
 
 
-// ---------------------------------------------------------------------------
-// CTA-pair variant (two SMs per tile, tcgen05 cta_group::2), used when N % 256 == 0.
-//
-// A pair of CTAs in a (2,1,1) cluster owns a 256 x 256 grad_w tile: CTA r holds
-// rows 128r..128r+127 of the tile (its A operand, its TMEM accumulator) and
-// columns 128r..128r+127 of the B operand.  The even CTA issues one
-// tcgen05.mma.cta_group::2 (M=256, N=256, K=32) per 32-token block; each SM then
-// reads 4 KB of A and 4 KB of B from its own shared memory per MMA instead of
-// 4 KB + 8 KB, which is what bounds the single-SM kernel.  Both CTAs' TMA loads
-// count on the even CTA's full barriers; the even CTA's commits are multicast to
-// both CTAs' empty / accumulator-full barriers; both epilogues release the even
-// CTA's accumulator-empty barrier.
-constexpr int kPStages = 5;
-constexpr int kPABytes = 128 * BT;                  // 16 KB: this CTA's 128 rows of g^T
-constexpr int kPBBytes = 128 * BT;                  // 16 KB: this CTA's half of x^T
-constexpr int kPStageBytes = kPABytes + kPBBytes;   // 32 KB
-constexpr int kPOffOut = kPStages * kPStageBytes;
-constexpr int kPOffSf = kPOffOut + kOutBytes;
-constexpr int kPOffBar = kPOffSf + kPStages * kSfStage;
-constexpr int kPNumBars = 2 * kPStages + 3;
-constexpr int kPOffMisc = kPOffBar + kPNumBars * 8;
-constexpr int kPOffTable = kPOffMisc + 16;
-
-__host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
-  return static_cast<size_t>(kPOffTable) + sizeof(int) * (2 * static_cast<size_t>(E) + 2) +
-         sizeof(uint16_t) * static_cast<size_t>(E) + 1024;
-}
-static_assert(wgrad_pair_smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
-
-constexpr int kPThreads = 320;
-
-__global__ void __launch_bounds__(kPThreads, 1) grouped_wgrad_pair_kernel(const __grid_constant__ WgradArgs args) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const int E = args.E, N = args.N, K = args.K;
-  int* s_misc = reinterpret_cast<int*>(smem + kPOffMisc);  // [0] tmem base [1] abort [2] flag
-  int* s_off = reinterpret_cast<int*>(smem + kPOffTable);
-  int* s_pad = s_off + (E + 1);
-  uint16_t* s_order = reinterpret_cast<uint16_t*>(s_pad + (E + 1));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_misc[1]);
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const uint32_t lane = lane_id();
-  const uint32_t rank = cluster_ctarank();  // 0: issues the pair MMAs
-  const bool leader = rank == 0;
-
-  if (tid == 0) s_misc[1] = 0;
-  // Both CTAs see the same offsets, so both take the same branch here.
-  if (!load_offsets(args.expert_off, E, args.M, s_off, s_pad, &s_misc[2], args.status)) return;
-
-  for (int e = tid; e < E; e += kPThreads) {
-    const int ce = s_off[e + 1] - s_off[e];
-    int rank_e = 0;
-    for (int j = 0; j < E; ++j) {
-      const int cj = s_off[j + 1] - s_off[j];
-      rank_e += (cj > ce) || (cj == ce && j < e);
-    }
-    s_order[rank_e] = static_cast<uint16_t>(e);
-  }
-  const uint32_t bar0 = sbase + kPOffBar;
-  auto bar_full = [&](int st) { return bar0 + 8u * st; };             // used in CTA 0
-  auto bar_empty = [&](int st) { return bar0 + 8u * (kPStages + st); };
-  const uint32_t bar_acc_full = bar0 + 8u * (2 * kPStages);
-  const uint32_t bar_acc_empty = bar0 + 8u * (2 * kPStages + 1);     // used in CTA 0
-  const uint32_t bar_done = bar0 + 8u * (2 * kPStages + 2);
-  if (tid == 0) {
-    for (int st = 0; st < kPStages; ++st) {
-      mbar_init(bar_full(st), 1);
-      mbar_init(bar_empty(st), 1);
-    }
-    mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, 2 * kEpiWarps);
-    mbar_init(bar_done, 1);
-    fence_mbar_init();
-    tma_prefetch_desc(&args.tm_a);
-    tma_prefetch_desc(&args.tm_b);
-    tma_prefetch_desc(&args.tm_sfa);
-    tma_prefetch_desc(&args.tm_sfb);
-    tma_prefetch_desc(&args.tm_out);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(&s_misc[0]), kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
-  tc_fence_after();
-  const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
-
-  const int pairs_n = N / 256, tiles_k = K / BN;
-  const long long per_expert = static_cast<long long>(pairs_n) * tiles_k;
-  const long long total = per_expert * E;
-  const long long first = blockIdx.x >> 1, step = gridDim.x >> 1;
-  const uint32_t full0_leader = map_to_cta(bar_full(0), 0);
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int pending[kPStages];
-      uint32_t pending_phase[kPStages];
-      for (int st = 0; st < kPStages; ++st) pending[st] = 0, pending_phase[st] = 0;
-      bool ok = true;
-      for (long long it = first; it < total && ok; it += step) {
-        const int e = s_order[it / per_expert];
-        const int tile = static_cast<int>(it % per_expert);
-        const int np = tile / tiles_k, kt = tile % tiles_k;
-        const int cnt = s_off[e + 1] - s_off[e];
-        if (cnt == 0) continue;
-        const int nch = (cnt + BT - 1) / BT;
-        const int ch0 = s_pad[e] / BT;
-        const int arow = np * 256 + 128 * static_cast<int>(rank);   // this CTA's g^T rows
-        const int brow = kt * BN + 128 * static_cast<int>(rank);    // this CTA's x^T rows
-        for (int c = 0; c < nch; ++c) {
-          if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full0_leader + 8u * stage;  // CTA 0's full barrier
-          if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (kPStageBytes + kSfStage));
-          const uint32_t sa = sbase + stage * kPStageBytes;
-          const int ch = ch0 + c;
-          tma_load_2d_pair(sa, &args.tm_a, ch * BT, arow, fb);
-          tma_load_2d_pair(sa + kPABytes, &args.tm_b, ch * BT, brow, fb);
-          // scale atoms: rows of 256 bytes, an atom = 2 rows; x's two atoms are adjacent
-          const uint32_t ssf = sbase + kPOffSf + stage * kSfStage;
-          tma_load_2d_pair(ssf, &args.tm_sfa, 0, 2 * (ch * (N / 128) + arow / 128), fb);
-          tma_load_2d_pair(ssf + 512, &args.tm_sfb, 0, 2 * (ch * (K / 128) + 2 * kt), fb);
-          pending[stage] = 1;
-          pending_phase[stage] = phase;
-          if (++stage == kPStages) stage = 0, phase ^= 1u;
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        if (args.status) atomicOr(args.status, kDevTimeout);
-      }
-      // CTA 0 never leaves with copies still landing; CTA 1's copies count on CTA 0's
-      // barriers, which CTA 0's MMA issuer has waited for before the final cluster sync.
-      if (leader)
-        for (int st = 0; st < kPStages; ++st)
-          if (pending[st]) mbar_wait_drain(bar_full(st), pending_phase[st]);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer (CTA 0 only)
-    if (leader && lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      constexpr uint16_t kBoth = 0x3;
-      auto stage_scales = [&](int st, uint32_t ph) -> bool {
-        if (!mbar_wait_spin(bar_full(st), ph, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t ssf = sbase + kPOffSf + st * kSfStage;
-        const uint32_t tsf = tmem + kSfCol0 + 16u * st;
-        tmem_cp_32x128b_warpx4_pair(tsf, make_sdesc(ssf, 0, 128, 0));
-        tmem_cp_32x128b_warpx4_pair(tsf + 8, make_sdesc(ssf + 512, 0, 128, 0));
-        tmem_cp_32x128b_warpx4_pair(tsf + 12, make_sdesc(ssf + 1024, 0, 128, 0));
-        return true;
-      };
-      for (long long it = first; it < total && ok; it += step) {
-        const int e = s_order[it / per_expert];
-        const int cnt = s_off[e + 1] - s_off[e];
-        if (cnt == 0) continue;
-        const int nch = (cnt + BT - 1) / BT;
-        if (!stage_scales(stage, phase) || !mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int c = 0; c < nch; ++c) {
-          const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
-          const int rem = cnt - c * BT;
-          const int nkb = rem >= BT ? 4 : (rem + 31) / 32;
-          const uint32_t sa = sbase + stage * kPStageBytes;
-          for (int kb = 0; kb < nkb; ++kb) {
-            mma_mxf8_block32_pair(tmem, sdesc_kmajor_sw128(sa + 32 * kb),
-                                  sdesc_kmajor_sw128(sa + kPABytes + 32 * kb),
-                                  idesc_mxf8_e4m3(256, 256, kb, kb), tsf, tsf + 8, (c | kb) != 0);
-          }
-          const int cur = stage;
-          if (++stage == kPStages) stage = 0, phase ^= 1u;
-          if (c + 1 < nch && !stage_scales(stage, phase)) {
-            ok = false;
-            break;
-          }
-          mma_commit_pair(bar_empty(cur), kBoth);
-        }
-        if (!ok) break;
-        mma_commit_pair(bar_acc_full, kBoth);
-        acc_phase ^= 1u;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        if (args.status) atomicOr(args.status, kDevTimeout);
-      }
-      mma_commit_pair(bar_done, 0x1);
-      mbar_wait_drain(bar_done, 0);
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
-    const int quarter = warp & 3;
-    const int half = ew >> 2;
-    const int row = quarter * 32 + static_cast<int>(lane);
-    const bool store_leader = (ew == 0 && lane == 0);
-    const uint32_t acc_empty_leader = map_to_cta(bar_acc_empty, 0);
-    uint32_t acc_phase = 0;
-    for (long long it = first; it < total; it += step) {
-      const int e = s_order[it / per_expert];
-      const int tile = static_cast<int>(it % per_expert);
-      const int np = tile / tiles_k, kt = tile % tiles_k;
-      const int cnt = s_off[e + 1] - s_off[e];
-      uint32_t pk[64];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) pk[j] = 0u;
-      if (cnt > 0 && !*abort_flag) {
-        if (mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
-          tc_fence_after();
-          uint32_t r[128];
-          const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 128u * half;
-          tmem_ld_32x32b_x32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          tmem_ld_32x32b_x32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-          tmem_ld_32x32b_x32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-#pragma unroll
-          for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
-        } else {
-          *abort_flag = 1;
-          if (lane == 0 && args.status) atomicOr(args.status, kDevTimeout);
-        }
-        acc_phase ^= 1u;
-      }
-      const uint32_t stage_base = sbase + kPOffOut;
-      const int orow = e * N + np * 256 + 128 * static_cast<int>(rank);
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        if (store_leader) bulk_wait_read0();
-        named_bar_sync(1, kEpiWarps * 32);
-        if ((b >> 1) == half) {
-#pragma unroll
-          for (int chunk = 0; chunk < 8; ++chunk) {
-            const int jj = (b & 1) * 8 + chunk;
-            const uint32_t addr = stage_base + row * 128 + ((chunk ^ (row & 7)) << 4);
-            st_shared_v4(addr, pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
-          }
-          fence_async_smem();
-        }
-        named_bar_sync(1, kEpiWarps * 32);
-        if (store_leader && !*abort_flag) {
-          tma_store_2d(&args.tm_out, kt * BN + 64 * b, orow, stage_base);
-          bulk_commit();
-        }
-      }
-    }
-    if (store_leader) bulk_wait0();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // no pair MMA reads this CTA's smem or writes its TMEM any more
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
-}
-
 }  // namespace
 
-// The CTA-pair kernel is opt-in (MGW_WGRAD_CTA_PAIRS=1): on GB300 it measured slower
-// than the single-SM kernel on the 8192^3 x 8-expert workload (555 us against 464-475 us).
-bool wgrad_uses_pair(int N) {
-  const char* v = std::getenv("MGW_WGRAD_CTA_PAIRS");
-  return N % 256 == 0 && v != nullptr && v[0] == '1';
-}
-
 cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream) {
-  static thread_local int attr_set_device = -1;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static thread_local uint64_t attr_ctx = 0;
+  const cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(grouped_wgrad_kernel),
+                                             wgrad_smem_bytes(kMaxExperts), &attr_ctx);
   if (err != cudaSuccess) return err;
-  if (attr_set_device != dev) {
-    err = cudaFuncSetAttribute(grouped_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(wgrad_smem_bytes(kMaxExperts)));
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(grouped_wgrad_pair_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(wgrad_pair_smem_bytes(kMaxExperts)));
-    if (err != cudaSuccess) return err;
-    attr_set_device = dev;
-  }
-  if (!wgrad_uses_pair(a.N)) {
-    const long long total = static_cast<long long>(a.N / BM) * (a.K / BN) * a.E;
-    long long grid = num_sms;
-    if (grid > total) grid = total;
-    if (grid < 1) grid = 1;
-    grouped_wgrad_kernel<<<static_cast<unsigned>(grid), kThreads, wgrad_smem_bytes(a.E), stream>>>(a);
-    return cudaGetLastError();
-  }
-  // One CTA pair per two SMs, as many pairs as fit at once.
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kPThreads, 1, 1);
-  cfg.dynamicSmemBytes = wgrad_pair_smem_bytes(a.E);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  static thread_local int clusters_device = -1;
-  static thread_local int max_clusters = 0;
-  if (clusters_device != dev) {
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    cfg.dynamicSmemBytes = wgrad_pair_smem_bytes(kMaxExperts);
-    err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_wgrad_pair_kernel, &cfg);
-    if (err != cudaSuccess) return err;
-    if (max_clusters < 1) return cudaErrorLaunchOutOfResources;
-    clusters_device = dev;
-    cfg.dynamicSmemBytes = wgrad_pair_smem_bytes(a.E);
-  }
-  const long long total = static_cast<long long>(a.N / 256) * (a.K / BN) * a.E;
-  long long pairs = max_clusters;
-  if (pairs > total) pairs = total;
-  if (pairs < 1) pairs = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  err = cudaLaunchKernelEx(&cfg, grouped_wgrad_pair_kernel, a);
-  if (err != cudaSuccess) return err;
+  const long long total = static_cast<long long>(a.N / BM) * (a.K / BN) * a.E;
+  long long grid = num_sms;
+  if (grid > total) grid = total;
+  if (grid < 1) grid = 1;
+  grouped_wgrad_kernel<<<static_cast<unsigned>(grid), kThreads, wgrad_smem_bytes(a.E), stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -570,17 +570,11 @@ size_t balanced_workspace_bytes(int slots) {
 
 cudaError_t launch_grouped_wgrad_balanced(WgradArgs a, void* workspace, int slots, int num_sms,
                                           cudaStream_t stream) {
-  static thread_local int attr_set_device = -1;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static thread_local uint64_t attr_ctx = 0;
+  cudaError_t err = set_smem_attr_once(
+      reinterpret_cast<const void*>(grouped_wgrad_balanced_kernel),
+      balanced_smem_bytes(kMaxBalancedExperts), &attr_ctx);
   if (err != cudaSuccess) return err;
-  if (attr_set_device != dev) {
-    err = cudaFuncSetAttribute(grouped_wgrad_balanced_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(balanced_smem_bytes(kMaxBalancedExperts)));
-    if (err != cudaSuccess) return err;
-    attr_set_device = dev;
-  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.ws_sched = reinterpret_cast<int*>(ws);
   a.ws_cnt = reinterpret_cast<int*>(ws + kWsHeaderBytes);

@@ -47,6 +47,40 @@ _lock = threading.Lock()
 _lib = None
 
 
+def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declares the C ABI's argument and return types on a loaded build of the library."""
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.mgw_status_string.argtypes = [I]
+    lib.mgw_status_string.restype = ctypes.c_char_p
+    lib.mgw_version.argtypes = []
+    lib.mgw_version.restype = I
+    lib.mgw_mxfp8_token_capacity.argtypes = [I, I]
+    lib.mgw_mxfp8_token_capacity.restype = SZ
+    lib.mgw_mxfp8_scale_bytes.argtypes = [I, SZ]
+    lib.mgw_mxfp8_scale_bytes.restype = SZ
+    lib.mgw_mxfp8_quantize.argtypes = [P, I, I, P, I, P, P, SZ, I, P, P]
+    lib.mgw_mxfp8_quantize.restype = I
+    lib.mgw_mxfp8_quantize_gather.argtypes = [P, I, P, I, I, P, I, P, P, SZ, I, P, P]
+    lib.mgw_mxfp8_quantize_gather.restype = I
+    lib.mgw_grouped_wgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
+    lib.mgw_grouped_wgrad_mxfp8.restype = I
+    lib.mgw_grouped_dgrad_f32.argtypes = [P, P, P, I, I, I, I, P, P, P]
+    lib.mgw_grouped_dgrad_f32.restype = I
+    lib.mgw_mxfp8_quantize_rows.argtypes = [P, I, P, I, I, P, I, P, P, SZ, I, P, P]
+    lib.mgw_mxfp8_quantize_rows.restype = I
+    lib.mgw_grouped_fprop_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
+    lib.mgw_grouped_fprop_mxfp8.restype = I
+    lib.mgw_grouped_dgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
+    lib.mgw_grouped_dgrad_mxfp8.restype = I
+    lib.mgw_grouped_wgrad_mxfp8_balanced.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, SZ, P, P]
+    lib.mgw_grouped_wgrad_mxfp8_balanced.restype = I
+    lib.mgw_grouped_wgrad_workspace_bytes.argtypes = [I, I, I]
+    lib.mgw_grouped_wgrad_workspace_bytes.restype = SZ
+    lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
+    lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.restype = I
+    return lib
+
+
 def load() -> ctypes.CDLL:
     """Load libmgw.so (built in-tree by ``moe_grouped_gemm_wgrad_gb300.build``)."""
     global _lib
@@ -55,38 +89,8 @@ def load() -> ctypes.CDLL:
             return _lib
         if not os.path.exists(LIB_PATH):
             raise MgwError(f"{LIB_PATH} is not built; run `python -m moe_grouped_gemm_wgrad_gb300.build`")
-        lib = ctypes.CDLL(LIB_PATH)
-        P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-        lib.mgw_status_string.argtypes = [I]
-        lib.mgw_status_string.restype = ctypes.c_char_p
-        lib.mgw_version.argtypes = []
-        lib.mgw_version.restype = I
-        lib.mgw_mxfp8_token_capacity.argtypes = [I, I]
-        lib.mgw_mxfp8_token_capacity.restype = SZ
-        lib.mgw_mxfp8_scale_bytes.argtypes = [I, SZ]
-        lib.mgw_mxfp8_scale_bytes.restype = SZ
-        lib.mgw_mxfp8_quantize.argtypes = [P, I, I, P, I, P, P, SZ, I, P, P]
-        lib.mgw_mxfp8_quantize.restype = I
-        lib.mgw_mxfp8_quantize_gather.argtypes = [P, I, P, I, I, P, I, P, P, SZ, I, P, P]
-        lib.mgw_mxfp8_quantize_gather.restype = I
-        lib.mgw_grouped_wgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
-        lib.mgw_grouped_wgrad_mxfp8.restype = I
-        lib.mgw_grouped_dgrad_f32.argtypes = [P, P, P, I, I, I, I, P, P, P]
-        lib.mgw_grouped_dgrad_f32.restype = I
-        lib.mgw_mxfp8_quantize_rows.argtypes = [P, I, P, I, I, P, I, P, P, SZ, I, P, P]
-        lib.mgw_mxfp8_quantize_rows.restype = I
-        lib.mgw_grouped_fprop_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
-        lib.mgw_grouped_fprop_mxfp8.restype = I
-        lib.mgw_grouped_dgrad_mxfp8.argtypes = [P, P, P, P, P, I, I, I, I, SZ, SZ, P, P, P]
-        lib.mgw_grouped_dgrad_mxfp8.restype = I
-        lib.mgw_grouped_wgrad_mxfp8_balanced.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, SZ, P, P]
-        lib.mgw_grouped_wgrad_mxfp8_balanced.restype = I
-        lib.mgw_grouped_wgrad_workspace_bytes.argtypes = [I, I, I]
-        lib.mgw_grouped_wgrad_workspace_bytes.restype = SZ
-        lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
-        lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.restype = I
-        _lib = lib
-        return lib
+        _lib = bind(ctypes.CDLL(LIB_PATH))
+        return _lib
 
 
 def _check(st: int, what: str) -> None:

@@ -294,3 +294,104 @@ def grouped_dgrad_mx(dyq, dys, wtq, wts, expert_off, w_off, M: int) -> np.ndarra
     _load().orc_grouped_dgrad_mx(_ptr(dyq), _ptr(dys), _ptr(wtq), _ptr(wts), _ptr(off),
                                  _ptr(woff), E, M, N, K, Mcap, Mw, _ptr(out))
     return out
+
+
+# ------------------------------------------------ full-size references by matmul
+# The same definitions, for outputs too large for the loops above: each expert's operands
+# are decoded exactly into fp64 with this oracle's own E4M3 and E8M0 decoders (per byte,
+# and per 32-element block for the scale), and numpy's fp64 matrix product forms the sums.
+# A product of two decoded MXFP8 values is exact in fp64, so these differ from the loop
+# versions only in the order of the fp64 additions (pinned against them on small cases).
+_tables = None
+
+
+def _decode_tables():
+    """(E4M3 value of every byte, E8M0 value of every byte), from the decoders above."""
+    global _tables
+    if _tables is None:
+        _tables = (np.array([e4m3_decode(b) for b in range(256)], dtype=np.float64),
+                   np.array([e8m0_decode(b) for b in range(256)], dtype=np.float64))
+    return _tables
+
+
+def dequantize_token_axis(q, sc, t0: int, count: int) -> np.ndarray:
+    """fp64 [C, count]: columns t0 .. t0+count-1 of a token-axis operand (q [C, Mcap],
+    plain scales sc [C, Mcap/32]) decoded and multiplied by their 32-token block's scale.
+    t0 is a multiple of 32 (an expert's padded start)."""
+    e4m3, e8m0 = _decode_tables()
+    assert t0 % 32 == 0
+    vals = e4m3[q[:, t0:t0 + count]]
+    nb = (count + 31) // 32
+    scale = e8m0[sc[:, t0 // 32:t0 // 32 + nb]]
+    vals *= np.repeat(scale, 32, axis=1)[:, :count]
+    return vals
+
+
+def dequantize_rows(q, sc, p0: int, count: int) -> np.ndarray:
+    """fp64 [count, C]: rows p0 .. p0+count-1 of a row-wise operand (q [Mcap, C], plain
+    scales sc [Mcap, C/32]) decoded and multiplied by their 32-column block's scale."""
+    e4m3, e8m0 = _decode_tables()
+    vals = e4m3[q[p0:p0 + count]]
+    vals *= np.repeat(e8m0[sc[p0:p0 + count]], 32, axis=1)
+    return vals
+
+
+def grouped_wgrad_by_expert(gq, gs, xq, xs, expert_off):
+    """Yields (e, fp64 grad_w[e] [N, K]) for every expert: the wgrad page's per-expert
+    g_e^T x_e over its tokens, as a matrix product of the decoded slices.  An expert
+    without tokens yields None (its rows are zero by definition)."""
+    off = _off(expert_off)
+    P = padded_starts(off)
+    for e in range(off.size - 1):
+        c = int(off[e + 1] - off[e])
+        if c == 0:
+            yield e, None
+            continue
+        G = dequantize_token_axis(gq, gs, int(P[e]), c)
+        X = dequantize_token_axis(xq, xs, int(P[e]), c)
+        yield e, G @ X.T
+
+
+def grouped_dgrad_by_expert(dy: np.ndarray, W: np.ndarray, expert_off):
+    """Yields (e, r0, r1, dx[r0:r1] fp64, bound[r0:r1] fp64) for every expert with rows:
+    the dgrad page's dx[r] = dy[r] . W[e(r)] for the rows the expert owns, and
+    bound = |dy| . |W[e]|."""
+    off = _off(expert_off)
+    for e in range(off.size - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        d = dy[r0:r1].astype(np.float64)
+        w = W[e].astype(np.float64)
+        yield e, r0, r1, d @ w, np.abs(d) @ np.abs(w)
+
+
+def grouped_fprop_mx_by_expert(xq, xs, wq, ws, expert_off, w_off):
+    """Yields (e, r0, r1, y[r0:r1] fp64) for every expert with rows: the forward
+    y[r, n] = deq(x)[r] . deq(W)[e, n] of :func:`grouped_fprop_mx` as a matrix product."""
+    off, woff = _off(expert_off), _off(w_off)
+    P, Pw = padded_starts(off), padded_starts(woff)
+    N = int(woff[1] - woff[0])
+    for e in range(off.size - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        X = dequantize_rows(xq, xs, int(P[e]), r1 - r0)
+        Wd = dequantize_rows(wq, ws, int(Pw[e]), N)
+        yield e, r0, r1, X @ Wd.T
+
+
+def grouped_dgrad_mx_by_expert(dyq, dys, wtq, wts, expert_off, w_off):
+    """Yields (e, r0, r1, dx[r0:r1] fp64) for every expert with rows: the MXFP8 data
+    gradient dx[r, k] = sum_n deq(dy)[r, n] deq(W)[e, n, k] of :func:`grouped_dgrad_mx`
+    as a matrix product."""
+    off, woff = _off(expert_off), _off(w_off)
+    P, Pw = padded_starts(off), padded_starts(woff)
+    N = int(woff[1] - woff[0])
+    for e in range(off.size - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        D = dequantize_rows(dyq, dys, int(P[e]), r1 - r0)
+        Wt = dequantize_token_axis(wtq, wts, int(Pw[e]), N)
+        yield e, r0, r1, D @ Wt.T

@@ -7,7 +7,8 @@ import torch
 
 import oracle
 from moe_grouped_gemm_wgrad_gb300 import mgw, synth
-from helpers import atoms_to_plain, bf16_to_f64, dev_bf16, dev_i32, wgrad_tol
+from helpers import (atoms_to_plain, bf16_to_f64, check_rows_full, dev_bf16, dev_i32, full_case,
+                     oracle_quantize_by_expert, wgrad_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -198,8 +199,8 @@ def test_dgrad_mx_matches_oracle(counts, N, K):
     assert (err <= tol).all(), f"max excess {np.max(err - tol)}"
 
 
-def test_fprop_more_items_than_sms_sampled():
-    """~270 items over the SMs: every CTA takes several; checked on sampled elements."""
+def test_fprop_more_items_than_sms():
+    """~270 items over the SMs: every CTA takes several; every output element checked."""
     rng = np.random.default_rng(31)
     counts = synth.multinomial_counts(rng, 8192, 8)
     N, K = 1024, 256
@@ -207,18 +208,7 @@ def test_fprop_more_items_than_sms_sampled():
     y, _, _ = _run_fprop(x, W, off, w_off, N)
     xq, xs = oracle.mxfp8_quantize_rows(x, off)
     wq, ws = oracle.mxfp8_quantize_rows(W, w_off)
-    P, Pw = oracle.padded_starts(off), oracle.padded_starts(w_off)
-    got = bf16_to_f64(y)
-    rs = rng.integers(0, x.shape[0], 300)
-    ns = rng.integers(0, N, 300)
-    refs = []
-    for r, n in zip(rs, ns):
-        e = oracle.expert_for_row_bsearch(off, int(r))
-        p = P[e] + r - off[e]
-        refs.append(oracle.mx_dot(xq[p], xs[p], wq[Pw[e] + n], ws[Pw[e] + n]))
-    refs = np.array(refs)
-    rms = float(np.sqrt(np.mean(refs ** 2)))
-    assert (np.abs(got[rs, ns] - refs) <= wgrad_tol(refs, rms)).all()
+    check_rows_full(y, oracle.grouped_fprop_mx_by_expert(xq, xs, wq, ws, off, w_off), x.shape[0], N)
 
 
 def test_fprop_no_rows_and_bad_offsets():
@@ -247,60 +237,46 @@ def test_fprop_no_rows_and_bad_offsets():
 
 
 @pytest.mark.slow
-def test_moe_ffn_pair_forward_and_mx_dgrad_full_size_sampled():
+def test_moe_ffn_pair_forward_and_mx_dgrad_full_size():
     """The MoE FFN pair at full size (65536 routed rows of 8192 tokens over 64 experts,
     hidden 4096, ffn 1536): forward y = x W[e]^T with x gathered from the hidden states,
-    and dx = dy W[e], both in MXFP8, checked on sampled elements against the oracle
-    (which quantizes just the sampled rows and columns)."""
-    wg, dg = synth.moe_ffn_pair()
+    and dx = dy W[e], both in MXFP8.  Every quantized operand is compared bit for bit with
+    the oracle's, and every output element with the oracle's per-expert product (rms over
+    the whole output)."""
+    wg, dg = full_case("moe_ffn_pair"), full_case("moe_ffn_pair.dgrad")
     off = wg.expert_off
     E, N, K = wg.E, wg.N, wg.K              # N = ffn 1536, K = hidden 4096
     M = wg.M
-    hidden = wg.meta["hidden_bf16"]
-    tok = wg.meta["token_of_row"]
     Wb = synth.bf16_bits_from_f32(dg.W.reshape(E * N, K))
     w_off = synth.offsets_from_counts(np.full(E, N))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     d_off = dev_i32(off)
-    xq, xs = mgw.mxfp8_quantize_rows(dev_bf16(hidden), d_off, status=status, row_index=dev_i32(tok))
+    Mcap = mgw.token_capacity(M, E)
+    xq, xs = mgw.mxfp8_quantize_rows(dev_bf16(wg.meta["hidden_bf16"]), d_off, Mcap, status=status,
+                                     row_index=dev_i32(wg.meta["token_of_row"]))
     Wd = dev_bf16(Wb)
     wq, ws = mgw.mxfp8_quantize_rows(Wd, dev_i32(w_off), status=status)
     y = mgw.grouped_fprop_mxfp8(xq, xs, wq, ws, d_off, M, N, status=status)
-    dyq, dys = mgw.mxfp8_quantize_rows(dev_bf16(wg.g_bf16), d_off, status=status)
+    dyq, dys = mgw.mxfp8_quantize_rows(dev_bf16(wg.g_bf16), d_off, Mcap, status=status)
     wtq, wts = mgw.mxfp8_quantize(Wd, dev_i32(w_off), status=status)
     dx = mgw.grouped_dgrad_mxfp8(dyq, dys, wtq, wts, d_off, M, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    P, Pw = oracle.padded_starts(off), oracle.padded_starts(w_off)
-    rng = np.random.default_rng(77)
-    rs = rng.integers(0, M, 96)
-    # forward samples
-    xq_h, ys = xq.cpu().numpy(), bf16_to_f64(y)
-    refs, got = [], []
-    for r in rs:
-        e = oracle.expert_for_row_bsearch(off, int(r))
-        p = P[e] + r - off[e]
-        oq, osc = oracle.mxfp8_quantize_rows(hidden[tok[r]][None, :], [0, 1])
-        assert np.array_equal(xq_h[p], oq[0])  # the gathered row, bit-exact
-        for n in rng.integers(0, N, 3):
-            wq_o, ws_o = oracle.mxfp8_quantize_rows(Wb[e * N + n][None, :], [0, 1])
-            refs.append(oracle.mx_dot(oq[0], osc[0], wq_o[0], ws_o[0]))
-            got.append(ys[r, n])
-    refs, got = np.array(refs), np.array(got)
-    assert (np.abs(got - refs) <= wgrad_tol(refs, float(np.sqrt(np.mean(refs ** 2))))).all()
-    # data-gradient samples
-    dxs = bf16_to_f64(dx)
-    W3 = Wb.reshape(E, N, K)
-    refs, got = [], []
-    for r in rs:
-        e = oracle.expert_for_row_bsearch(off, int(r))
-        dq, dsc = oracle.mxfp8_quantize_rows(wg.g_bf16[r][None, :], [0, 1])
-        for k in rng.integers(0, K, 3):
-            cq, csc = oracle.mxfp8_quantize(np.ascontiguousarray(W3[e][:, k:k + 1]), [0, N])
-            refs.append(oracle.mx_dot(dq[0], dsc[0], cq[0, :N], csc[0, :N // 32]))
-            got.append(dxs[r, k])
-    refs, got = np.array(refs), np.array(got)
-    assert (np.abs(got - refs) <= wgrad_tol(refs, float(np.sqrt(np.mean(refs ** 2))))).all()
+    del Wd
+    Mw, Mw2 = wq.shape[0], wtq.shape[1]
+    oxq, oxs = oracle_quantize_by_expert(wg.x_bf16, off, Mcap, rows=True)
+    owq, ows = oracle_quantize_by_expert(Wb, w_off, Mw, rows=True)
+    assert np.array_equal(xq.cpu().numpy(), oxq) and np.array_equal(wq.cpu().numpy(), owq)
+    assert np.array_equal(atoms_to_plain(xs.cpu().numpy(), Mcap, K), oxs)
+    assert np.array_equal(atoms_to_plain(ws.cpu().numpy(), Mw, K), ows)
+    del xq, wq
+    check_rows_full(y, oracle.grouped_fprop_mx_by_expert(oxq, oxs, owq, ows, off, w_off), M, N)
+    del oxq, owq
+    odq, ods = oracle_quantize_by_expert(wg.g_bf16, off, Mcap, rows=True)
+    owtq, owts = oracle_quantize_by_expert(Wb, w_off, Mw2)
+    assert np.array_equal(dyq.cpu().numpy(), odq) and np.array_equal(wtq.cpu().numpy(), owtq)
+    assert np.array_equal(atoms_to_plain(wts.cpu().numpy(), K, Mw2), owts)
+    check_rows_full(dx, oracle.grouped_dgrad_mx_by_expert(odq, ods, owtq, owts, off, w_off), M, K)
 
 
 def test_forward_and_mx_dgrad_max_experts():

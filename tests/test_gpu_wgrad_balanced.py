@@ -7,7 +7,8 @@ import torch
 
 import oracle
 from moe_grouped_gemm_wgrad_gb300 import mgw, synth
-from helpers import bf16_to_f64, dev_bf16, dev_i32, wgrad_tol
+from helpers import (bf16_to_f64, check_wgrad_full, dev_bf16, dev_i32, full_case,
+                     full_oracle_operands, oracle_quantize_by_expert, wgrad_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -122,41 +123,25 @@ def test_balanced_no_tokens_and_bad_offsets(ws):
     assert _counters_zero(ws)
 
 
-def test_balanced_matches_static_kernel_sampled(ws):
-    """More items than SMs, checked on sampled elements against the oracle."""
+def test_balanced_matches_oracle_more_items_than_sms(ws):
+    """More items than SMs (1024 x 2048 per expert), one long expert split, every output
+    element against the oracle."""
     case = synth.wgrad_random(6000, 1024, 2048, [5000, 0, 900, 100], seed=49)
-    off, gq, gs, xq, xs = ops = _operands(case)
-    out = _run(case, ws, ops)
-    ogq, ogs = oracle.mxfp8_quantize(case.g_bf16, case.expert_off)
-    oxq, oxs = oracle.mxfp8_quantize(case.x_bf16, case.expert_off)
-    rng = np.random.default_rng(50)
-    counts = np.diff(case.expert_off)
-    nz = np.nonzero(counts > 0)[0]
-    es, ns, ks = rng.choice(nz, 1500), rng.integers(0, case.N, 1500), rng.integers(0, case.K, 1500)
-    ref = np.array([oracle.grouped_wgrad_element(ogq, ogs, oxq, oxs, case.expert_off, int(e), int(n), int(k))
-                    for e, n, k in zip(es, ns, ks)])
-    got = bf16_to_f64(out[torch.as_tensor(es * case.N + ns, device="cuda"), torch.as_tensor(ks, device="cuda")])
-    assert (np.abs(got - ref) <= wgrad_tol(ref)).all()
-    assert not bool(out.view(case.E, case.N, case.K)[1].float().abs().amax())
+    out = _run(case, ws)
+    ops = oracle_quantize_by_expert(case.g_bf16, case.expert_off, mgw.token_capacity(case.M, case.E))
+    ops += oracle_quantize_by_expert(case.x_bf16, case.expert_off, mgw.token_capacity(case.M, case.E))
+    check_wgrad_full(out, ops, case.expert_off, case.N, case.K)
+    assert _counters_zero(ws)
 
 
 @pytest.mark.slow
-def test_balanced_skewed_workload_full_size_sampled(ws):
-    case = synth.wgrad_skew()
+def test_balanced_skewed_workload_full_size(ws):
+    """The skewed-routing workload (27 of 32 experts empty, one expert of 12544 tokens
+    split over token ranges): every output element against the oracle, rms over the whole
+    output, one element per output tile from the plain loop oracle."""
+    case = full_case("wgrad_skew")
     out = _run(case, ws)
-    ogq, ogs = oracle.mxfp8_quantize(case.g_bf16, case.expert_off)
-    oxq, oxs = oracle.mxfp8_quantize(case.x_bf16, case.expert_off)
-    rng = np.random.default_rng(51)
-    counts = np.diff(case.expert_off)
-    nz = np.nonzero(counts > 0)[0]
-    es, ns, ks = rng.choice(nz, 2000), rng.integers(0, case.N, 2000), rng.integers(0, case.K, 2000)
-    ref = np.array([oracle.grouped_wgrad_element(ogq, ogs, oxq, oxs, case.expert_off, int(e), int(n), int(k))
-                    for e, n, k in zip(es, ns, ks)])
-    got = bf16_to_f64(out[torch.as_tensor(es * case.N + ns, device="cuda"), torch.as_tensor(ks, device="cuda")])
-    assert (np.abs(got - ref) <= wgrad_tol(ref, float(np.sqrt(np.mean(ref ** 2))))).all()
-    full = out.view(case.E, case.N, case.K)
-    empty = torch.as_tensor(np.nonzero(counts == 0)[0], device="cuda")
-    assert not bool(full[empty].float().abs().amax())
+    check_wgrad_full(out, full_oracle_operands("wgrad_skew"), case.expert_off, case.N, case.K)
     assert _counters_zero(ws)
 
 

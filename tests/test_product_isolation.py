@@ -35,3 +35,15 @@ def test_missing_library_raises(monkeypatch):
         mgw.load()
     with pytest.raises(mgw.MgwError):
         mgw.token_capacity(10, 2)
+
+
+def test_time_limit_test_switch_only_in_the_test_build():
+    """The device time-limit test drops a pipeline stage through MGW_TEST_DROP_LOAD; only the
+    test build of the library reads that variable, libmgw.so does not contain it."""
+    from moe_grouped_gemm_wgrad_gb300 import build
+
+    build.build()
+    with open(build.LIB, "rb") as f:
+        assert b"MGW_TEST_DROP_LOAD" not in f.read()
+    with open(build.LIB_TESTHOOKS, "rb") as f:
+        assert b"MGW_TEST_DROP_LOAD" in f.read()

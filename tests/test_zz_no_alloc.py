@@ -1,13 +1,16 @@
-"""The no-allocation entry point of the load-balanced wgrad (library-owned workspace): the
-oracle's result within 8e-3 |ref| + 1e-3 rms(ref), identical from call to call, and no
-device memory taken by repeated calls.  Collected last, after every other GPU test."""
+"""The no-allocation entry point of the load-balanced wgrad, for callers that cannot
+allocate device memory (it runs on a workspace the library owns): the same result as the
+entry points that take caller memory, within 8e-3 |ref| + 1e-3 rms(ref), on calls made
+back to back; the oracle's result; identical from call to call; no device memory taken by
+repeated calls.  Collected last, after every other GPU test, and self-contained, so it
+also passes alone in a fresh process."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from moe_grouped_gemm_wgrad_gb300 import mgw, synth
-from helpers import bf16_to_f64, dev_bf16, dev_i32, wgrad_tol
+from helpers import bf16_to_f64, check_wgrad_full, dev_bf16, dev_i32, oracle_quantize_by_expert, wgrad_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -60,3 +63,36 @@ def test_noalloc_single_tile_split_many_ways():
     xq, xs = oracle.mxfp8_quantize(case.x_bf16, case.expert_off)
     ref = oracle.grouped_wgrad(gq, gs, xq, xs, case.expert_off)
     assert (np.abs(got - ref) <= wgrad_tol(ref)).all()
+
+
+def test_noalloc_matches_caller_workspace_entry_points_on_consecutive_calls():
+    """Two no-allocation calls in a row against the balanced entry point with a caller
+    workspace and the static entry point, on operands with a split expert."""
+    case = synth.wgrad_random(7000, 256, 512, [4000, 0, 2900, 100], seed=63)
+    off, gq, gs, xq, xs = ops = _operands(case)
+    shape = (case.E * case.N, case.K)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = mgw.wgrad_workspace(case.E, case.N, case.K)
+    ref_bal = mgw.grouped_wgrad_mxfp8_balanced(gq, gs, xq, xs, off, case.M, ws, status=status)
+    ref_static = mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, case.M, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rb, rs = bf16_to_f64(ref_bal), bf16_to_f64(ref_static)
+    for _ in range(2):
+        got = bf16_to_f64(_call(case, ops, torch.empty(shape, dtype=torch.bfloat16, device="cuda")))
+        assert (np.abs(got - rb) <= wgrad_tol(rb)).all()
+        assert (np.abs(got - rs) <= wgrad_tol(rs)).all()
+
+
+def test_noalloc_more_than_64_tiles_per_expert_schedules_without_splits():
+    """2048 x 2048 per expert is 128 output tiles: splitting any expert would need more than
+    the library workspace's 128 partial slots, so no expert is split and the call runs on
+    the dynamic schedule alone.  Every output element against the oracle."""
+    case = synth.wgrad_random(6200, 2048, 2048, [6000, 0, 200], seed=64)
+    ops = _operands(case)
+    out = torch.full((case.E * case.N, case.K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _call(case, ops, out)
+    Mcap = mgw.token_capacity(case.M, case.E)
+    oops = oracle_quantize_by_expert(case.g_bf16, case.expert_off, Mcap)
+    oops += oracle_quantize_by_expert(case.x_bf16, case.expert_off, Mcap)
+    check_wgrad_full(out, oops, case.expert_off, case.N, case.K)
