@@ -77,7 +77,7 @@ class ClockSampler:
 
         self.proc = None
         self.path = path
-        self.window = None
+        self.windows = {}
         self.lines = []
         try:
             if cmd is None:
@@ -97,10 +97,12 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line)
 
-    def mark(self, t0: float, t1: float):
-        self.window = (t0, t1)
+    def mark(self, t0: float, t1: float, name: str = "step"):
+        self.windows[name] = (t0, t1)
 
     def stop(self):
+        """Stops sampling; returns {window name: summary} (the summary of all samples under
+        "all" when no window saw a sample)."""
         if self.proc is None:
             return None
         time.sleep(0.2)
@@ -125,14 +127,22 @@ class ClockSampler:
                 rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
             except ValueError:
                 continue
-        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
-        use = inside if inside else rows
-        if not use:
-            return None
-        reasons = sorted({n for r in use for n, v in zip(self.NAMES, r[4]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "power_w_median": statistics.median(r[3] for r in use), "reasons": reasons,
-                "samples": len(use), "samples_in_timed_window": len(inside)}
+
+        def summary(use, n_inside):
+            if not use:
+                return None
+            reasons = sorted({n for r in use for n, v in zip(self.NAMES, r[4]) if v.lower() == "active"})
+            return {"sm_mhz": statistics.median(r[1] for r in use),
+                    "sm_max_mhz": max(r[2] for r in use),
+                    "power_w_median": statistics.median(r[3] for r in use), "reasons": reasons,
+                    "samples": len(use), "samples_in_timed_window": n_inside}
+
+        out = {}
+        for name, (t0, t1) in self.windows.items():
+            inside = [r for r in rows if t0 <= r[0] <= t1]
+            out[name] = summary(inside if inside else rows, len(inside))
+        out["all"] = summary(rows, 0)
+        return out
 
 
 # ----------------------------------------------------------------- workloads
@@ -152,7 +162,7 @@ def dgrad_case(name):
     return getattr(synth, name)()
 
 
-def run_wgrad(name, steps, warmup, dist_ctx, clocks_csv=None):
+def run_wgrad(name, steps, warmup, dist_ctx, clocks_csv=None, clock_leg_s=0.6):
     import torch
 
     from moe_grouped_gemm_wgrad_gb300 import mgw
@@ -216,9 +226,37 @@ def run_wgrad(name, steps, warmup, dist_ctx, clocks_csv=None):
         ev[i][3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
-    clocks.mark(host_t0, time.time())
+    clocks.mark(host_t0, time.time(), "step")
     dist_ctx.barrier()
-    clk = clocks.stop()
+    # Clock leg: the wgrad kernel alone, back to back for at least `clock_leg_s` seconds,
+    # so that its time carries SM clock samples taken while it ran (the step region above
+    # can be shorter than the sampling period).
+    leg = None
+    if clock_leg_s > 0:
+        per = max(1, int(clock_leg_s / 4 / max(statistics.mean(e[2].elapsed_time(e[3]) for e in ev) * 1e-3, 1e-6)))
+        la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_leg = 0
+        torch.cuda.synchronize()
+        h0 = time.time()
+        la.record(stream)
+        while time.time() - h0 < clock_leg_s:
+            for _ in range(per):
+                mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)
+            n_leg += per
+            torch.cuda.synchronize()
+        lb.record(stream)
+        torch.cuda.synchronize()
+        clocks.mark(h0, time.time(), "wgrad_clock_leg")
+        leg = {"launches": n_leg, "ms_per_launch": la.elapsed_time(lb) / n_leg,
+               "seconds": la.elapsed_time(lb) * 1e-3}
+    clk_all = clocks.stop()
+    clk = clk_all.get("step") if clk_all else None
+    if leg is not None and clk_all:
+        c = clk_all.get("wgrad_clock_leg")
+        leg["clocks"] = c
+        if c:
+            leg["tflops"] = flops / (leg["ms_per_launch"] * 1e-3) / 1e12
+            leg["us_x_mhz"] = leg["ms_per_launch"] * 1e3 * c["sm_mhz"]
     total_ms = dist_ctx.max(t_start.elapsed_time(t_end))
     wg_ms = [e[2].elapsed_time(e[3]) for e in ev]
     qg_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -303,7 +341,7 @@ def run_wgrad(name, steps, warmup, dist_ctx, clocks_csv=None):
         "case": case, "flops": flops, "ms_per_step": ms_step, "wgrad_ms": wg_avg,
         "wgrad_ms_median": statistics.median(wg_ms), "quant_g_ms": statistics.mean(qg_ms),
         "quant_x_ms": statistics.mean(qx_ms), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-        "clocks": clk, "launches": 3 * steps, "x_gather": gather,
+        "clocks": clk, "clock_leg": leg, "launches": 3 * steps, "x_gather": gather,
         "quant_bytes": bytes_q(N) + bytes_q(K),
         "wgrad_min_bytes": N * Mcap + K * Mcap + (N + K) * Mcap // 32 + E * N * K * 2,
     }
@@ -463,6 +501,116 @@ def run_wgrad_kernels(name, steps, warmup):
     return res
 
 
+def run_wgrad_step_leg(name, steps, warmup):
+    """One workload's whole wgrad step -- quantize g, quantize x (gathered from the hidden
+    states by the routing map when the workload has one), grouped wgrad -- with CUDA events
+    around each launch, steps back to back.  For the tiny workload the step time is
+    dominated by launch latency; for the larger ones the output exceeds L2."""
+    import torch
+
+    from moe_grouped_gemm_wgrad_gb300 import mgw
+
+    case = wgrad_case(name)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M, N, K, E = case.M, case.N, case.K, case.E
+    off = torch.from_numpy(case.expert_off).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    Mcap = mgw.token_capacity(M, E)
+    g = torch.from_numpy(case.g_bf16.view(np.int16)).to(dev).view(torch.bfloat16)
+    gather = "hidden_bf16" in case.meta
+    if gather:
+        x = torch.from_numpy(case.meta["hidden_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+        rows = torch.from_numpy(case.meta["token_of_row"]).to(dev)
+    else:
+        x = torch.from_numpy(case.x_bf16.view(np.int16)).to(dev).view(torch.bfloat16)
+    gq = torch.empty((N, Mcap), dtype=torch.uint8, device=dev)
+    xq = torch.empty((K, Mcap), dtype=torch.uint8, device=dev)
+    gs = torch.empty((mgw.scale_bytes(N, Mcap),), dtype=torch.uint8, device=dev)
+    xs = torch.empty((mgw.scale_bytes(K, Mcap),), dtype=torch.uint8, device=dev)
+    out = torch.empty((E * N, K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ks = [lambda: mgw.mxfp8_quantize(g, off, Mcap, gq, gs, status),
+          (lambda: mgw.mxfp8_quantize_gather(x, rows, off, Mcap, xq, xs, status)) if gather
+          else (lambda: mgw.mxfp8_quantize(x, off, Mcap, xq, xs, status)),
+          lambda: mgw.grouped_wgrad_mxfp8(gq, gs, xq, xs, off, M, out, status)]
+    for _ in range(warmup):
+        for k in ks:
+            k()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ks) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, k in enumerate(ks):
+            k()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(ks))]
+    step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev)
+    flops = 2.0 * M * N * K
+    wg_bytes = N * Mcap + K * Mcap + (N + K) * Mcap // 32 + E * N * K * 2
+    return {"workload": case.name, "M": M, "N": N, "K": K, "experts": E,
+            "x": "gathered from hidden[token_of_row]" if gather else "materialised",
+            "kernels_ms": {"mxfp8_quantize_g": ms[0],
+                           "mxfp8_quantize_gather_x" if gather else "mxfp8_quantize_x": ms[1],
+                           "grouped_wgrad": ms[2]},
+            "step_ms": step_ms, "step_tflops": flops / (step_ms * 1e-3) / 1e12,
+            "wgrad_tflops": flops / (ms[2] * 1e-3) / 1e12,
+            "wgrad_hbm_gbs": wg_bytes / (ms[2] * 1e-3) / 1e9, "wgrad_algorithmic_bytes": wg_bytes,
+            "launches_per_step": len(ks)}
+
+
+def measure_dense_peaks(n: int = 8192, reps: int = 10):
+    """Dense GEMM rates of the vendor library on this GPU at n^3, best of ``reps`` with CUDA
+    events after three warm-up calls: block-scaled MXFP8 (torch._scaled_mm on e4m3 operands
+    with one e8m0 scale per 32 elements of K), TF32 (fp32 torch.matmul with TF32 allowed)
+    and bf16.  These are denominators for the roofline fractions, measured beside them."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flops = 2.0 * n ** 3
+    res = {"n": n, "how": f"best of {reps}, CUDA events, {n}^3, torch {torch.__version__}"}
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            t.append((a, b))
+        torch.cuda.synchronize()
+        return flops / (min(a.elapsed_time(b) for a, b in t) * 1e-3) / 1e12
+
+    A = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    B = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    res["bf16_tflops"] = best(lambda: A @ B)
+    a8 = A.to(torch.float8_e4m3fn)
+    b8 = B.to(torch.float8_e4m3fn).t().contiguous().t()
+    try:
+        e8 = torch.float8_e8m0fnu
+        sa = torch.full((n * (n // 32),), 127, dtype=torch.uint8, device=dev).view(e8)
+        sb = torch.full((n * (n // 32),), 127, dtype=torch.uint8, device=dev).view(e8)
+        res["mxfp8_tflops"] = best(lambda: torch._scaled_mm(a8, b8, sa, sb, out_dtype=torch.bfloat16))
+    except Exception as exc:  # an older torch without block-scaled MXFP8
+        res["mxfp8_error"] = repr(exc)[:200]
+    del a8, b8
+    Af, Bf = A.float(), B.float()
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        res["tf32_tflops"] = best(lambda: Af @ Bf)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    del A, B, Af, Bf
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ CPU baseline
 def oracle_wgrad_sample(case, n_sub: int, k_sub: int):
     """Times the oracle (as it stands, single thread) on expert 0's tokens for an
@@ -546,17 +694,27 @@ def main():
     ap.add_argument("--impl", choices=["mgw", "reference"], default="mgw")
     ap.add_argument("--workload", default="wgrad_8192",
                     choices=["wgrad_tiny", "wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
-    ap.add_argument("--dgrad-workload", default="dgrad_4096", choices=["dgrad_4096", "moe_ffn_pair", "none"])
+    ap.add_argument("--dgrad-workloads", default="dgrad_4096,moe_ffn_pair",
+                    help="comma list of fp32 dgrad legs (dgrad_4096, moe_ffn_pair) or none")
+    ap.add_argument("--wgrad-step-workloads", default="wgrad_tiny,moe_ffn_pair",
+                    help="comma list of extra whole-step wgrad legs (wgrad_tiny, wgrad_skew, "
+                         "moe_ffn_pair) or none")
     ap.add_argument("--mx-workload", default="moe_ffn_pair", choices=["moe_ffn_pair", "moe_ffn_small", "none"])
     ap.add_argument("--skew-workload", default="wgrad_skew",
                     choices=["wgrad_skew", "wgrad_8192", "moe_ffn_pair", "none"])
+    ap.add_argument("--clock-leg-s", type=float, default=0.6,
+                    help="seconds of back-to-back wgrad launches timed under clock sampling (0: off)")
+    ap.add_argument("--no-peak-probe", action="store_true",
+                    help="skip measuring the vendor library's MXFP8 / TF32 / bf16 GEMM rates")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None,
                     help="also write the raw nvidia-smi clock samples of the timed step to this CSV")
     args = ap.parse_args()
     peaks = _peaks()
-    # nominal fp8 : bf16 dense ratio 4.5 : 2.25; the sustained figure applies to a kernel
-    # timed inside a long loop (the default timed region runs about a second under load)
+    # Contract denominators: the measured bf16 dense rate times the nominal fp8 : bf16 (4.5 :
+    # 2.25) and tf32 : bf16 (1.1 : 2.25, taken as 1/2) ratios; the sustained figure applies to
+    # a kernel timed inside a long loop.  The vendor library's own MXFP8 and TF32 rates,
+    # measured in this run, are reported beside them.
     mxfp8_burst = 2.0 * peaks["bf16_tflops"]
     mxfp8_sustained = 2.0 * (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"])
     metric = "MXFP8 grouped wgrad TFLOP/s"
@@ -597,16 +755,21 @@ def main():
     from moe_grouped_gemm_wgrad_gb300 import build as _build
 
     _build.build()  # no-op when current
-    r = run_wgrad(args.workload, args.steps, args.warmup, d, args.clocks_csv)
-    dg = None
-    if args.dgrad_workload != "none":
-        dg = run_dgrad(args.dgrad_workload, max(5, min(args.steps, 50)), max(3, args.warmup))
+    lst = lambda v: [w for w in v.split(",") if w and w != "none"]  # noqa: E731
+    r = run_wgrad(args.workload, args.steps, args.warmup, d, args.clocks_csv, args.clock_leg_s)
+    legs_steps, legs_warm = max(5, min(args.steps, 50)), max(3, args.warmup)
+    dgs = {w: run_dgrad(w, legs_steps, legs_warm) for w in lst(args.dgrad_workloads)}
+    wsteps = {w: run_wgrad_step_leg(w, max(5, min(args.steps, 100 if w == "wgrad_tiny" else 20)), legs_warm)
+              for w in lst(args.wgrad_step_workloads)}
     sk = None
     if args.skew_workload != "none":
-        sk = run_wgrad_kernels(args.skew_workload, max(5, min(args.steps, 50)), max(3, args.warmup))
+        sk = run_wgrad_kernels(args.skew_workload, legs_steps, legs_warm)
     mx = None
     if args.mx_workload != "none":
-        mx = run_mx_pair(args.mx_workload, max(5, min(args.steps, 20)), max(3, args.warmup))
+        mx = run_mx_pair(args.mx_workload, max(5, min(args.steps, 20)), legs_warm)
+    dense = None
+    if not args.no_peak_probe:
+        dense = measure_dense_peaks()
     case = r["case"]
     value = r["flops"] * d.world / (r["ms_per_step"] * 1e-3) / 1e12
     wg_tflops = r["flops"] / (r["wgrad_ms"] * 1e-3) / 1e12
@@ -614,10 +777,26 @@ def main():
     power_capped = bool(r["clocks"]) and "sw_power_cap" in r["clocks"].get("reasons", [])
     peak_kind = "sustained" if (long_region or power_capped) else "burst"
     mxfp8_peak = mxfp8_sustained if peak_kind == "sustained" else mxfp8_burst
+    tf32_peak = peaks["bf16_tflops"] / 2.0
+    mx_meas = (dense or {}).get("mxfp8_tflops")
+    tf32_meas = (dense or {}).get("tf32_tflops")
     cpu = None
     if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
     if d.rank == 0:
+        note = (f"peak = 2 x measured bf16 dense ({peaks['source']}, MEASURED_PEAKS): burst "
+                f"{mxfp8_burst:.1f}, sustained {mxfp8_sustained:.1f} TFLOP/s (fp8:bf16 nominal 2)")
+        if mx_meas:
+            note += (f"; measured in this run: cuBLAS MXFP8 (torch._scaled_mm, e8m0 32-blocks) "
+                     f"{mx_meas:.1f}, cuBLAS TF32 {tf32_meas:.1f} TFLOP/s at 8192^3")
+        roof = {"bound": "tensor", "achieved": wg_tflops, "peak": mxfp8_peak,
+                "unit": "TFLOP/s", "frac": wg_tflops / mxfp8_peak,
+                "traffic": _traffic("grouped_wgrad_kernel", ["wgrad.cu", "ptx.cuh", "common.cuh"]),
+                "kernel": "grouped_wgrad_kernel", "peak_kind": peak_kind,
+                "frac_of_burst": wg_tflops / mxfp8_burst,
+                "algorithmic_bytes": r["wgrad_min_bytes"], "peak_note": note}
+        if mx_meas:
+            roof["frac_of_measured_mxfp8"] = wg_tflops / mx_meas
         line = {
             "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": d.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
@@ -628,36 +807,74 @@ def main():
                                 if r["x_gather"] else "mxfp8_quantize(g) + mxfp8_quantize(x) + grouped_wgrad_mxfp8"),
                        "l2": "inputs larger than L2 (bf16 g,x 2x134 MB; grad_w 1.07 GB per step)",
                        "parallelism": f"replicas x{d.world} (independent workloads, no collective)"},
-            "roofline": {"bound": "tensor", "achieved": wg_tflops, "peak": mxfp8_peak,
-                         "unit": "TFLOP/s", "frac": wg_tflops / mxfp8_peak,
-                         "traffic": _traffic("grouped_wgrad_kernel", ["wgrad.cu", "ptx.cuh", "common.cuh"]),
-                         "kernel": "grouped_wgrad_kernel", "peak_kind": peak_kind,
-                         "frac_of_burst": wg_tflops / mxfp8_burst,
-                         "algorithmic_bytes": r["wgrad_min_bytes"],
-                         "peak_note": f"2 x measured bf16 dense ({peaks['source']}): burst {mxfp8_burst:.1f}, "
-                                      f"sustained {mxfp8_sustained:.1f} TFLOP/s; fp8:bf16 nominal ratio 2"},
+            "roofline": roof,
             "kernels_ms": {"mxfp8_quantize_g": r["quant_g_ms"], "mxfp8_quantize_x": r["quant_x_ms"],
                            "grouped_wgrad": r["wgrad_ms"], "grouped_wgrad_median": r["wgrad_ms_median"]},
             "quantize_hbm": {"achieved_gbs": r["quant_bytes"] / ((r["quant_g_ms"] + r["quant_x_ms"]) * 1e-3) / 1e9,
-                             "peak_gbs": peaks["hbm_gbs"]},
+                             "peak_gbs": peaks["hbm_gbs"],
+                             "frac": r["quant_bytes"] / ((r["quant_g_ms"] + r["quant_x_ms"]) * 1e-3) / 1e9 / peaks["hbm_gbs"]},
             "e2e": {"value": r["flops"] * d.world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
             "cpu_baseline": cpu,
         }
-        if dg is not None:
-            tf32_peak = peaks["bf16_tflops"] / 2.0  # nominal tf32 : bf16 dense ratio 1.1 : 2.25
+        if r.get("clock_leg"):
+            leg = r["clock_leg"]
+            if leg.get("tflops"):
+                leg["frac"] = leg["tflops"] / mxfp8_sustained
+                leg["frac_note"] = "against the sustained denominator (a long back-to-back loop)"
+            line["wgrad_clock_leg"] = leg
+        if dense is not None:
+            line["dense_peaks_measured"] = dense
+        for w, dg in dgs.items():
             dg["roofline"] = {"bound": "tensor", "tf32_work_tflops": 3 * dg["tflops"], "peak": tf32_peak,
                               "unit": "TFLOP/s", "frac": 3 * dg["tflops"] / tf32_peak,
-                              "note": "3xTF32: three tf32 MMAs per fp32 product"}
-            line["dgrad"] = dg
+                              "note": "3xTF32: three tf32 MMAs per fp32 product; peak = measured bf16 / 2"}
+            if tf32_meas:
+                dg["roofline"]["frac_of_measured_tf32"] = 3 * dg["tflops"] / tf32_meas
+            line["dgrad" if w == "dgrad_4096" else f"dgrad_{w}"] = dg
+        for w, ws_ in wsteps.items():
+            ws_["wgrad_frac_of_burst"] = ws_["wgrad_tflops"] / mxfp8_burst
+            if mx_meas:
+                ws_["wgrad_frac_of_measured_mxfp8"] = ws_["wgrad_tflops"] / mx_meas
+            ws_["wgrad_hbm_frac"] = ws_["wgrad_hbm_gbs"] / peaks["hbm_gbs"]
+            line[f"wgrad_step_{w}"] = ws_
         if sk is not None:
+            for k in ("static", "balanced"):
+                sk[k]["hbm_frac"] = sk[k]["hbm_gbs"] / peaks["hbm_gbs"]
+                sk[k]["tensor_frac_of_burst"] = sk[k]["tflops"] / mxfp8_burst
             line["wgrad_static_vs_balanced"] = sk
         if mx is not None:
             for key in ("fprop_tflops", "dgrad_mx_tflops"):
                 mx[key.replace("tflops", "frac_of_burst")] = mx[key] / mxfp8_burst
+                if mx_meas:
+                    mx[key.replace("tflops", "frac_of_measured_mxfp8")] = mx[key] / mx_meas
             line["mx_forward_dgrad"] = mx
+        # the five workload configurations, one line each
+        cfgs = {"wgrad_8192": {"wgrad_ms": r["wgrad_ms"], "wgrad_tflops": wg_tflops,
+                               "frac_of_burst": wg_tflops / mxfp8_burst}}
+        if "wgrad_tiny" in wsteps:
+            t = wsteps["wgrad_tiny"]
+            cfgs["wgrad_tiny"] = {"step_ms": t["step_ms"], "wgrad_ms": t["kernels_ms"]["grouped_wgrad"],
+                                  "wgrad_tflops": t["wgrad_tflops"], "bound": "launch latency"}
+        if "dgrad_4096" in dgs:
+            cfgs["dgrad_4096"] = {"ms": dgs["dgrad_4096"]["ms"], "tflops_fp32": dgs["dgrad_4096"]["tflops"],
+                                  "frac_tf32": dgs["dgrad_4096"]["roofline"]["frac"]}
+        if sk is not None and sk["workload"] == "wgrad_skew":
+            cfgs["wgrad_skew"] = {"static_ms": sk["static"]["ms"], "balanced_ms": sk["balanced"]["ms"],
+                                  "balanced_hbm_frac": sk["balanced"]["hbm_frac"]}
+        if "moe_ffn_pair" in wsteps or "moe_ffn_pair" in dgs:
+            m = {}
+            if "moe_ffn_pair" in wsteps:
+                t = wsteps["moe_ffn_pair"]
+                m.update({"wgrad_ms": t["kernels_ms"]["grouped_wgrad"], "wgrad_tflops": t["wgrad_tflops"],
+                          "wgrad_frac_of_burst": t["wgrad_frac_of_burst"]})
+            if "moe_ffn_pair" in dgs:
+                m.update({"dgrad_f32_ms": dgs["moe_ffn_pair"]["ms"], "dgrad_f32_tflops": dgs["moe_ffn_pair"]["tflops"],
+                          "dgrad_f32_frac_tf32": dgs["moe_ffn_pair"]["roofline"]["frac"]})
+            cfgs["moe_ffn_pair"] = m
+        line["configs"] = cfgs
         print(json.dumps(line))
     d.close()
 

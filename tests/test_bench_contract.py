@@ -88,9 +88,14 @@ def test_clock_sampler_summarises_the_timed_window_without_a_csv():
     deadline = time.time() + 30
     while len(sampler.lines) < 2000 + len(lines) and time.time() < deadline:
         time.sleep(0.05)
-    sampler.mark(now - 10, now + 10)
-    clk = sampler.stop()
-    assert clk is not None
+    sampler.mark(now - 10, now + 10)                  # the timed step ("step")
+    sampler.mark(now - 4.85, now - 4.65, "leg")       # a second window: samples 2 and 3
+    summary = sampler.stop()
+    assert summary is not None
+    leg = summary["leg"]
+    assert leg["samples_in_timed_window"] == 2 and leg["sm_mhz"] == 1952.5
+    assert summary["all"]["samples"] == 7
+    clk = summary["step"]
     assert clk["samples_in_timed_window"] == 5 and clk["samples"] == 5
     assert clk["sm_mhz"] == 1952.0 and clk["sm_max_mhz"] == 2070.0
     assert clk["reasons"] == ["sw_power_cap"]

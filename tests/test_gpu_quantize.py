@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from moe_grouped_gemm_wgrad_gb300 import mgw, synth
-from helpers import atoms_to_plain, dev_bf16, dev_i32
+from helpers import atoms_to_plain, dev_bf16, dev_i32, full_case, full_oracle_operands
 
 pytestmark = pytest.mark.gpu
 
@@ -77,23 +77,33 @@ def test_quantize_special_values():
     _check(bits, [0, 100, 256])
 
 
+def _assert_equal(q, sc, oq, osc, C, Mcap):
+    bad = np.argwhere(q != oq)
+    assert bad.size == 0, f"{len(bad)} e4m3 bytes differ, first at {bad[:5].tolist()}"
+    bad = np.argwhere(atoms_to_plain(sc, C, Mcap) != osc)
+    assert bad.size == 0, f"{len(bad)} scale bytes differ, first at {bad[:5].tolist()}"
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
 def test_quantize_full_size_workloads(name):
-    case = synth.moe_ffn_pair()[0] if name == "moe_ffn_pair" else getattr(synth, name)()
-    _check(case.g_bf16, case.expert_off)
-    _check(case.x_bf16, case.expert_off)
+    """Every byte of both operands of the full-size workloads (x of the MoE FFN pair also
+    gathered straight from the hidden states by the routing map) against the oracle's
+    quantization of the same workload."""
+    case = full_case(name)
+    gq, gs, xq, xs = full_oracle_operands(name)
+    q, sc, Mcap = _run(case.g_bf16, case.expert_off)
+    _assert_equal(q, sc, gq, gs, case.N, Mcap)
+    q, sc, _ = _run(case.x_bf16, case.expert_off)
+    _assert_equal(q, sc, xq, xs, case.K, Mcap)
     if "hidden_bf16" in case.meta:  # x gathered from the hidden states by the routing map
-        Mcap = mgw.token_capacity(case.M, case.E)
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         q, sc = mgw.mxfp8_quantize_gather(dev_bf16(case.meta["hidden_bf16"]),
                                           dev_i32(case.meta["token_of_row"]),
                                           dev_i32(case.expert_off), Mcap=Mcap, status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        oq, osc = oracle.mxfp8_quantize(case.x_bf16, case.expert_off, Mcap)
-        assert np.array_equal(q.cpu().numpy(), oq)
-        assert np.array_equal(atoms_to_plain(sc.cpu().numpy(), case.K, Mcap), osc)
+        _assert_equal(q.cpu().numpy(), sc.cpu().numpy(), xq, xs, case.K, Mcap)
 
 
 def test_quantize_bad_offsets_reported_and_output_untouched():
