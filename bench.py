@@ -773,9 +773,9 @@ def main():
     case = r["case"]
     value = r["flops"] * d.world / (r["ms_per_step"] * 1e-3) / 1e12
     wg_tflops = r["flops"] / (r["wgrad_ms"] * 1e-3) / 1e12
+    # the sustained denominator for a timed region of half a second or more, else burst
     long_region = r["ms_per_step"] * args.steps >= 500.0
-    power_capped = bool(r["clocks"]) and "sw_power_cap" in r["clocks"].get("reasons", [])
-    peak_kind = "sustained" if (long_region or power_capped) else "burst"
+    peak_kind = "sustained" if long_region else "burst"
     mxfp8_peak = mxfp8_sustained if peak_kind == "sustained" else mxfp8_burst
     tf32_peak = peaks["bf16_tflops"] / 2.0
     mx_meas = (dense or {}).get("mxfp8_tflops")

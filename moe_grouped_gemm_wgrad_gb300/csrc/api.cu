@@ -272,18 +272,26 @@ mgw_status wgrad_check(const void* gq, const void* gs, const void* xq, const voi
   return MGW_OK;
 }
 
-// Tensor maps and sizes of the wgrad kernels.
+// Tensor maps and sizes of the wgrad kernels; `pair` selects the CTA-pair layout (x^T boxes
+// of 128 rows, scale atoms loaded by TMA).
 bool wgrad_maps(mgw::WgradArgs* a, const void* gq, const void* gs, const void* xq,
                 const void* xs, const int32_t* expert_off, int E, int M, int N, int K,
-                size_t Mcap, void* out_bf16, int* status_dev) {
+                size_t Mcap, void* out_bf16, int* status_dev, bool pair) {
   std::memset(a, 0, sizeof(*a));
   if (!make_map_2d(&a->tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, Mcap, N, Mcap, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&a->tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128, 256,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&a->tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, Mcap, K, Mcap, 128,
+                   pair ? 128 : 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&a->tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_bf16, K,
                    static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return false;
+  if (pair && (!make_map_2d(&a->tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, 256,
+                            static_cast<uint64_t>(N) * (Mcap / 32) / 256, 256, 256, 2,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+               !make_map_2d(&a->tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, 256,
+                            static_cast<uint64_t>(K) * (Mcap / 32) / 256, 256, 256, 4,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)))
     return false;
   a->out = out_bf16;
   a->gs = static_cast<const uint8_t*>(gs);
@@ -325,7 +333,7 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced(const void* gq, const void* gs, cons
   st = current_device(&dev);
   if (st != MGW_OK) return st;
   mgw::WgradArgs a;
-  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev, false))
     return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_grouped_wgrad_balanced(a, workspace, slots, dev.sms,
                                                              static_cast<cudaStream_t>(stream));
@@ -353,7 +361,7 @@ mgw_status mgw_grouped_wgrad_mxfp8_balanced_noalloc(const void* gq, const void* 
   if (cudaMemsetAsync(ws, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MGW_ERR_CUDA;
   mgw::WgradArgs a;
-  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev, false))
     return MGW_ERR_CUDA;
   const cudaError_t err = mgw::launch_grouped_wgrad_balanced(a, ws, slots, dev.sms,
                                                              static_cast<cudaStream_t>(stream));
@@ -370,7 +378,8 @@ mgw_status mgw_grouped_wgrad_mxfp8(const void* gq, const void* gs, const void* x
   mgw_status st = current_device(&dev);
   if (st != MGW_OK) return st;
   mgw::WgradArgs a;
-  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev))
+  if (!wgrad_maps(&a, gq, gs, xq, xs, expert_off, E, M, N, K, Mcap, out_bf16, status_dev,
+                  mgw::wgrad_uses_pair(E, N)))
     return MGW_ERR_CUDA;
 #ifdef MGW_TEST_HOOKS
   {

@@ -9,6 +9,9 @@
 namespace mgw {
 
 constexpr int kMaxExperts = 1024;
+// Experts the CTA-pair wgrad kernel takes (its expert tables share shared memory with a
+// six-stage ring); more experts, or N % 256 != 0, use the single-SM kernel.
+constexpr int kMaxPairExperts = 512;
 
 size_t quantize_smem_bytes(int E);
 // tm_src: bf16 [M, C] source, box 128 features x 128 tokens, no swizzle.
@@ -30,9 +33,15 @@ uint64_t current_context_id();
 // Sets the kernel's maximum dynamic shared memory once per context and calling thread.
 cudaError_t set_smem_attr_once(const void* kernel, size_t bytes, uint64_t* done_ctx);
 
+// True when the static wgrad runs on CTA pairs (tcgen05 cta_group::2): then tm_b's box
+// is 128 rows (each CTA holds half of the 256-column tile) and tm_sfa / tm_sfb are used.
+bool wgrad_uses_pair(int E, int N);
+
 struct WgradArgs {
   CUtensorMap tm_a;    // g^T e4m3 [N, Mcap], box 128 tokens x 128 rows, 128B swizzle
-  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x 256 rows, 128B swizzle
+  CUtensorMap tm_b;    // x^T e4m3 [K, Mcap], box 128 tokens x 256 rows (128 for pairs), 128B swizzle
+  CUtensorMap tm_sfa;  // CTA pairs: g scale atoms as 256-byte rows, box 256 x 2 (one atom)
+  CUtensorMap tm_sfb;  // CTA pairs: x scale atoms as 256-byte rows, box 256 x 4 (two atoms)
   CUtensorMap tm_out;  // grad_w bf16 [E*N, K], box 64 cols x 128 rows, 128B swizzle
   void* out;           // grad_w (plain stores of the zero tiles)
   const uint8_t* gs;   // g scale atoms

@@ -379,18 +379,356 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
 }
 
 
+
+// ---------------------------------------------------------------------------
+// CTA-pair kernel (two SMs per output tile, tcgen05 cta_group::2), used when N % 256 == 0.
+//
+// A pair of CTAs in a (2,1,1) cluster owns a 256 x 256 grad_w tile: CTA r holds rows
+// 128r .. 128r+127 of the tile (its A operand, its TMEM accumulator) and columns
+// 128r .. 128r+127 of the B operand; the even CTA issues one
+// tcgen05.mma.cta_group::2.kind::mxf8f6f4 (M=256, N=256, K=32) per 32-token block, which
+// reads A from each CTA's shared memory and B from both halves.  Per 128-token chunk each
+// SM then takes in 32 KB by TMA and reads 8 KB per MMA from its shared memory, against
+// 48 KB and 12 KB for the single-SM tile of the same work per SM: the single-SM kernel's
+// TMA writes plus tensor-core reads exceed what one SM's shared memory serves at the full
+// MMA rate, the pair's stay within it.  The smaller stages also make the ring six deep.
+//
+// Both CTAs' TMA loads count on the even CTA's full barriers; the even CTA's commits are
+// multicast to both CTAs' empty / accumulator-full barriers; both epilogues release the
+// even CTA's accumulator-empty barrier.  Each CTA's producer ends by waiting until every
+// stage it filled has been released, so no copy is still landing when a CTA exits.
+constexpr int kPStages = 6;
+constexpr int kPABytes = 128 * BT;                  // 16 KB: this CTA's 128 rows of g^T
+constexpr int kPBBytes = 128 * BT;                  // 16 KB: this CTA's half of x^T
+constexpr int kPStageBytes = kPABytes + kPBBytes;   // 32 KB
+constexpr int kPOffOut = kPStages * kPStageBytes;
+constexpr int kPOffSf = kPOffOut + kOutBytes;
+constexpr int kPOffBar = kPOffSf + kPStages * kSfStage;
+constexpr int kPNumBars = 2 * kPStages + 3;        // full[], empty[], acc_full, acc_empty, done
+constexpr int kPOffMisc = (kPOffBar + kPNumBars * 8 + 15) & ~15;
+constexpr int kPOffTable = kPOffMisc + 16;
+
+__host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
+  return static_cast<size_t>(kPOffTable) + sizeof(int) * (2 * static_cast<size_t>(E) + 2) +
+         sizeof(uint16_t) * static_cast<size_t>(E) + 1024;
+}
+static_assert(wgrad_pair_smem_bytes(kMaxPairExperts) <= 232448, "shared memory budget");
+static_assert(kSfCol0 + 16 * kPStages <= kTmemCols, "TMEM budget");
+
+// The four pair MMAs (M=256, N=256, K=32 each) of one 128-token chunk, constant
+// instruction descriptors, the K step as +2 in the descriptors' start-address field.
+__device__ __forceinline__ void mma_mxf8_chunk128_pair(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                                       uint32_t sfa, uint32_t sfb,
+                                                       uint32_t accumulate) {
+  mma_mxf8_block32_pair(d, adesc, bdesc, idesc_mxf8_e4m3(256, 256, 0, 0), sfa, sfb, accumulate);
+  mma_mxf8_block32_pair(d, adesc + 2, bdesc + 2, idesc_mxf8_e4m3(256, 256, 1, 1), sfa, sfb, 1u);
+  mma_mxf8_block32_pair(d, adesc + 4, bdesc + 4, idesc_mxf8_e4m3(256, 256, 2, 2), sfa, sfb, 1u);
+  mma_mxf8_block32_pair(d, adesc + 6, bdesc + 6, idesc_mxf8_e4m3(256, 256, 3, 3), sfa, sfb, 1u);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_wgrad_pair_kernel(const __grid_constant__ WgradArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int E = args.E, N = args.N, K = args.K;
+  int* s_misc = reinterpret_cast<int*>(smem + kPOffMisc);  // [0] tmem base [1] abort [2] flag
+  int* s_off = reinterpret_cast<int*>(smem + kPOffTable);
+  int* s_pad = s_off + (E + 1);
+  uint16_t* s_order = reinterpret_cast<uint16_t*>(s_pad + (E + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_misc[1]);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair MMAs
+  const bool leader = rank == 0;
+
+  if (tid == 0) s_misc[1] = 0;
+  // Both CTAs read the same offsets, so both return here or neither does.
+  if (!load_offsets(args.expert_off, E, args.M, s_off, s_pad, &s_misc[2], args.status)) return;
+
+  for (int e = tid; e < E; e += kThreads) {
+    const int ce = s_off[e + 1] - s_off[e];
+    int rank_e = 0;
+    for (int j = 0; j < E; ++j) {
+      const int cj = s_off[j + 1] - s_off[j];
+      rank_e += (cj > ce) || (cj == ce && j < e);
+    }
+    s_order[rank_e] = static_cast<uint16_t>(e);
+  }
+  const uint32_t bar0 = sbase + kPOffBar;
+  auto bar_full = [&](int st) { return bar0 + 8u * st; };             // used in the even CTA
+  auto bar_empty = [&](int st) { return bar0 + 8u * (kPStages + st); };
+  const uint32_t bar_acc_full = bar0 + 8u * (2 * kPStages);
+  const uint32_t bar_acc_empty = bar0 + 8u * (2 * kPStages + 1);     // used in the even CTA
+  const uint32_t bar_done = bar0 + 8u * (2 * kPStages + 2);
+  if (tid == 0) {
+    for (int st = 0; st < kPStages; ++st) {
+      mbar_init(bar_full(st), 1);
+      mbar_init(bar_empty(st), 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 2 * kEpiWarps);
+    mbar_init(bar_done, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&args.tm_a);
+    tma_prefetch_desc(&args.tm_b);
+    tma_prefetch_desc(&args.tm_sfa);
+    tma_prefetch_desc(&args.tm_sfb);
+    tma_prefetch_desc(&args.tm_out);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&s_misc[0]), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
+  // The peer CTA's abort flag: a role that gives up tells both CTAs.
+  const uint32_t peer_abort = map_to_cta(smem_u32(&s_misc[1]), rank ^ 1u);
+  auto abort_both = [&]() {
+    *abort_flag = 1;
+    st_cluster_u32(peer_abort, 1u);
+    if (args.status) atomicOr(args.status, kDevTimeout);
+  };
+
+  const int pairs_n = N / 256, tiles_k = K / BN;
+  const int per_expert = pairs_n * tiles_k;  // 32-bit: the C ABI checks E x tiles < 2^31
+  const long long total = static_cast<long long>(per_expert) * E;
+  const long long npairs = gridDim.x >> 1;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int filled[kPStages];
+      uint32_t filled_phase[kPStages];
+      for (int st = 0; st < kPStages; ++st) filled[st] = 0, filled_phase[st] = 0;
+      bool ok = true;
+      const uint32_t full0_leader = map_to_cta(bar_full(0), 0);
+      ItemIter items{total, npairs, 0, pair};
+      long long it = 0;
+      while (ok && items.next(it)) {
+        const int e = s_order[static_cast<int>(it) / per_expert];
+        const int tile = static_cast<int>(it) % per_expert;
+        const int np = tile / tiles_k, kt = tile % tiles_k;
+        const int cnt = s_off[e + 1] - s_off[e];
+        if (cnt == 0) continue;
+        const int nch = (cnt + BT - 1) / BT;
+        const int ch0 = s_pad[e] / BT;
+        const int arow = np * 256 + 128 * static_cast<int>(rank);   // this CTA's g^T rows
+        const int brow = kt * BN + 128 * static_cast<int>(rank);    // this CTA's x^T rows
+        for (int c = 0; c < nch; ++c) {
+          if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (kPStageBytes + kSfStage));
+          const uint32_t fb = full0_leader + 8u * stage;  // the even CTA's full barrier
+          const uint32_t sa = sbase + stage * kPStageBytes;
+          const int ch = ch0 + c;
+          tma_load_2d_pair(sa, &args.tm_a, ch * BT, arow, fb);
+          tma_load_2d_pair(sa + kPABytes, &args.tm_b, ch * BT, brow, fb);
+          // scale atoms as rows of 256 bytes (an atom is 2 rows): this CTA's g atom and
+          // both x atoms of the K tile (every CTA's accumulator spans all 256 columns)
+          const uint32_t ssf = sbase + kPOffSf + stage * kSfStage;
+          tma_load_2d_pair(ssf, &args.tm_sfa, 0, 2 * (ch * (N / 128) + arow / 128), fb);
+          tma_load_2d_pair(ssf + 512, &args.tm_sfb, 0, 2 * (ch * (K / 128) + 2 * kt), fb);
+          filled[stage] = 1;
+          filled_phase[stage] = phase;
+          if (++stage == kPStages) stage = 0, phase ^= 1u;
+        }
+      }
+      if (!ok) abort_both();
+      // Every stage this CTA filled is released by the MMAs that read it (or, after an
+      // abort, the wait gives up after its time limit, long after any copy has landed).
+      for (int st = 0; st < kPStages; ++st)
+        if (filled[st]) mbar_wait_drain(bar_empty(st), filled_phase[st]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer (even CTA only)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      constexpr uint16_t kBoth = 0x3;
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
+      const uint64_t sf_desc0 = make_sdesc(sbase + kPOffSf, 0, 128, 0);
+      // Waits for the chunk in `st` to land in both CTAs and copies its scale atoms into
+      // each CTA's TMEM slot (each CTA from its own shared memory).
+      auto stage_scales = [&](int st, uint32_t ph) -> bool {
+        if (!mbar_wait_spin(bar_full(st), ph, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t dsf = sf_desc0 + static_cast<uint32_t>(st * (kSfStage >> 4));
+        const uint32_t tsf = tmem + kSfCol0 + 16u * st;
+        tmem_cp_32x128b_warpx4_pair(tsf, dsf);
+        tmem_cp_32x128b_warpx4_pair(tsf + 8, dsf + (512 >> 4));
+        tmem_cp_32x128b_warpx4_pair(tsf + 12, dsf + (1024 >> 4));
+        return true;
+      };
+      ItemIter items{total, npairs, 0, pair};
+      long long it = 0;
+      while (ok && items.next(it)) {
+        const int e = s_order[static_cast<int>(it) / per_expert];
+        const int cnt = s_off[e + 1] - s_off[e];
+        if (cnt == 0) continue;
+        const int nch = (cnt + BT - 1) / BT;
+        const int full_chunks = cnt / BT;
+        if (!stage_scales(stage, phase) ||
+            !mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int c = 0; c < nch; ++c) {
+          const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
+          const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (kPStageBytes >> 4));
+          const uint64_t bd = ad + (kPABytes >> 4);
+          if (c < full_chunks) {
+            mma_mxf8_chunk128_pair(tmem, ad, bd, tsf, tsf + 8, c != 0);
+          } else {
+            const int nkb = (cnt - c * BT + 31) / 32;
+            for (int kb = 0; kb < nkb; ++kb)
+              mma_mxf8_block32_pair(tmem, ad + 2 * kb, bd + 2 * kb, idesc_mxf8_e4m3(256, 256, kb, kb),
+                                    tsf, tsf + 8, (c | kb) != 0);
+          }
+          mma_commit_pair(bar_empty(stage), kBoth);
+          if (++stage == kPStages) stage = 0, phase ^= 1u;
+          if (c + 1 < nch && !stage_scales(stage, phase)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(bar_acc_full, kBoth);
+        acc_phase ^= 1u;
+      }
+      if (!ok) abort_both();
+      // All MMAs issued by this thread complete before TMEM is released.
+      mma_commit_pair(bar_done, 0x1);
+      mbar_wait_drain(bar_done, 0);
+    }
+  } else if (warp == kZeroWarp) {
+    // ------------------------ this CTA's rows of the tiles of experts without tokens
+    uint8_t* out = static_cast<uint8_t*>(args.out);
+    const size_t pitch = static_cast<size_t>(K) * 2;
+    ItemIter items{total, npairs, 0, pair};
+    long long it = 0;
+    while (items.next(it)) {
+      const int e = s_order[static_cast<int>(it) / per_expert];
+      if (s_off[e + 1] != s_off[e]) continue;
+      const int tile = static_cast<int>(it) % per_expert;
+      const int np = tile / tiles_k, kt = tile % tiles_k;
+      uint8_t* base = out + (static_cast<size_t>(e) * N + np * 256 + 128 * rank) * pitch +
+                      static_cast<size_t>(kt) * BN * 2 + lane * 16;
+#pragma unroll 4
+      for (int r = 0; r < BM; ++r)
+        *reinterpret_cast<uint4*>(base + r * pitch) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    const int row = quarter * 32 + static_cast<int>(lane);
+    const bool store_leader = (ew == 0 && lane == 0);
+    const uint32_t acc_empty_leader = map_to_cta(bar_acc_empty, 0);
+    uint32_t acc_phase = 0;
+    ItemIter items{total, npairs, 0, pair};
+    long long it = 0;
+    while (items.next(it)) {
+      const int e = s_order[static_cast<int>(it) / per_expert];
+      const int tile = static_cast<int>(it) % per_expert;
+      const int np = tile / tiles_k, kt = tile % tiles_k;
+      const int cnt = s_off[e + 1] - s_off[e];
+      if (cnt == 0) continue;  // written by the zero warp
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) pk[j] = 0u;
+      if (!*abort_flag) {
+        if (mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
+          tc_fence_after();
+          uint32_t r[128];
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 128u * half;
+          tmem_ld_32x32b_x32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_ld_32x32b_x32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+          tmem_ld_32x32b_x32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
+        } else if (lane == 0) {
+          abort_both();
+        }
+        acc_phase ^= 1u;
+      }
+      const uint32_t stage_base = sbase + kPOffOut;
+      const int orow = e * N + np * 256 + 128 * static_cast<int>(rank);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (store_leader) bulk_wait_read0();
+        named_bar_sync(1, kEpiWarps * 32);
+        if ((b >> 1) == half) {
+#pragma unroll
+          for (int chunk = 0; chunk < 8; ++chunk) {
+            const int jj = (b & 1) * 8 + chunk;
+            const uint32_t addr = stage_base + row * 128 + ((chunk ^ (row & 7)) << 4);
+            st_shared_v4(addr, pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+          }
+          fence_async_smem();
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (store_leader && !*abort_flag) {
+          tma_store_2d(&args.tm_out, kt * BN + 64 * b, orow, stage_base);
+          bulk_commit();
+        }
+      }
+    }
+    if (store_leader) bulk_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no pair MMA reads this CTA's shared memory or writes its TMEM any more
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
 }  // namespace
 
+bool wgrad_uses_pair(int E, int N) { return N % 256 == 0 && E <= kMaxPairExperts; }
+
 cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t stream) {
-  static thread_local uint64_t attr_ctx = 0;
-  const cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(grouped_wgrad_kernel),
-                                             wgrad_smem_bytes(kMaxExperts), &attr_ctx);
+  if (!wgrad_uses_pair(a.E, a.N)) {
+    static thread_local uint64_t attr_ctx = 0;
+    const cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(grouped_wgrad_kernel),
+                                               wgrad_smem_bytes(kMaxExperts), &attr_ctx);
+    if (err != cudaSuccess) return err;
+    const long long total = static_cast<long long>(a.N / BM) * (a.K / BN) * a.E;
+    long long grid = num_sms;
+    if (grid > total) grid = total;
+    if (grid < 1) grid = 1;
+    grouped_wgrad_kernel<<<static_cast<unsigned>(grid), kThreads, wgrad_smem_bytes(a.E), stream>>>(a);
+    return cudaGetLastError();
+  }
+  static thread_local uint64_t attr_ctx_pair = 0;
+  const cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(grouped_wgrad_pair_kernel),
+                                             wgrad_pair_smem_bytes(kMaxPairExperts), &attr_ctx_pair);
   if (err != cudaSuccess) return err;
-  const long long total = static_cast<long long>(a.N / BM) * (a.K / BN) * a.E;
-  long long grid = num_sms;
-  if (grid > total) grid = total;
-  if (grid < 1) grid = 1;
-  grouped_wgrad_kernel<<<static_cast<unsigned>(grid), kThreads, wgrad_smem_bytes(a.E), stream>>>(a);
+  // One CTA pair per two SMs (both dies have an even SM count), at most one pair per item.
+  const long long total = static_cast<long long>(a.N / 256) * (a.K / BN) * a.E;
+  long long pairs = num_sms / 2;
+  if (pairs > total) pairs = total;
+  if (pairs < 1) pairs = 1;
+  grouped_wgrad_pair_kernel<<<static_cast<unsigned>(2 * pairs), kThreads,
+                              wgrad_pair_smem_bytes(a.E), stream>>>(a);
   return cudaGetLastError();
 }
 
