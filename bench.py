@@ -501,7 +501,7 @@ def run_wgrad_kernels(name, steps, warmup):
     return res
 
 
-def run_wgrad_step_leg(name, steps, warmup):
+def run_wgrad_step_leg(name, steps, warmup, graph_steps=0):
     """One workload's whole wgrad step -- quantize g, quantize x (gathered from the hidden
     states by the routing map when the workload has one), grouped wgrad -- with CUDA events
     around each launch, steps back to back.  For the tiny workload the step time is
@@ -550,6 +550,33 @@ def run_wgrad_step_leg(name, steps, warmup):
     step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev)
     flops = 2.0 * M * N * K
     wg_bytes = N * Mcap + K * Mcap + (N + K) * Mcap // 32 + E * N * K * 2
+    graph = None
+    if graph_steps > 0:
+        # The same launches captured once into a CUDA graph and replayed: the device time
+        # of a step without the host's per-call work between launches.
+        cg = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for k in ks:  # one eager pass on the capture stream first
+                k()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(cg, stream=side):
+            for _ in range(graph_steps):
+                for k in ks:
+                    k()
+        cg.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cg.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in the graph replay")
+        gms = a.elapsed_time(b) / graph_steps
+        graph = {"steps_per_graph": graph_steps, "step_ms": gms,
+                 "step_tflops": flops / (gms * 1e-3) / 1e12}
     return {"workload": case.name, "M": M, "N": N, "K": K, "experts": E,
             "x": "gathered from hidden[token_of_row]" if gather else "materialised",
             "kernels_ms": {"mxfp8_quantize_g": ms[0],
@@ -558,7 +585,7 @@ def run_wgrad_step_leg(name, steps, warmup):
             "step_ms": step_ms, "step_tflops": flops / (step_ms * 1e-3) / 1e12,
             "wgrad_tflops": flops / (ms[2] * 1e-3) / 1e12,
             "wgrad_hbm_gbs": wg_bytes / (ms[2] * 1e-3) / 1e9, "wgrad_algorithmic_bytes": wg_bytes,
-            "launches_per_step": len(ks)}
+            "launches_per_step": len(ks), "cuda_graph": graph}
 
 
 def measure_dense_peaks(n: int = 8192, reps: int = 10):
@@ -759,7 +786,8 @@ def main():
     r = run_wgrad(args.workload, args.steps, args.warmup, d, args.clocks_csv, args.clock_leg_s)
     legs_steps, legs_warm = max(5, min(args.steps, 50)), max(3, args.warmup)
     dgs = {w: run_dgrad(w, legs_steps, legs_warm) for w in lst(args.dgrad_workloads)}
-    wsteps = {w: run_wgrad_step_leg(w, max(5, min(args.steps, 100 if w == "wgrad_tiny" else 20)), legs_warm)
+    wsteps = {w: run_wgrad_step_leg(w, max(5, min(args.steps, 100 if w == "wgrad_tiny" else 20)), legs_warm,
+                                    graph_steps=100 if w == "wgrad_tiny" else 0)
               for w in lst(args.wgrad_step_workloads)}
     sk = None
     if args.skew_workload != "none":
@@ -857,7 +885,8 @@ def main():
         if "wgrad_tiny" in wsteps:
             t = wsteps["wgrad_tiny"]
             cfgs["wgrad_tiny"] = {"step_ms": t["step_ms"], "wgrad_ms": t["kernels_ms"]["grouped_wgrad"],
-                                  "wgrad_tflops": t["wgrad_tflops"], "bound": "launch latency"}
+                                  "wgrad_tflops": t["wgrad_tflops"], "bound": "launch latency",
+                                  "graph_step_ms": (t["cuda_graph"] or {}).get("step_ms")}
         if "dgrad_4096" in dgs:
             cfgs["dgrad_4096"] = {"ms": dgs["dgrad_4096"]["ms"], "tflops_fp32": dgs["dgrad_4096"]["tflops"],
                                   "frac_tf32": dgs["dgrad_4096"]["roofline"]["frac"]}

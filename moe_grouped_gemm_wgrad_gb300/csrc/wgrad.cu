@@ -661,7 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+          if (lane == 0) mbar_arrive_remote(acc_empty_leader);
 #pragma unroll
           for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
         } else if (lane == 0) {
