@@ -59,18 +59,19 @@ mgw_status current_device(DeviceInfo* info) {
   return MGW_OK;
 }
 
-// 2-D tiled tensor map: `inner` contiguous elements per row, `outer` rows,
-// `pitch` bytes between rows.  A tensor map is plain data (base address, sizes, strides,
-// box and swizzle), so encoded maps are kept in a small process-wide table keyed by every
-// one of those inputs and reused by later calls on the same buffers.
+// A tensor map is plain data (base address, sizes, strides, box and swizzle), so encoded
+// maps are kept in a small process-wide table keyed by every one of those inputs and reused
+// by later calls on the same buffers.
 struct MapKey {
   const void* base;
-  uint64_t inner, outer, pitch;
-  uint32_t box_inner, box_outer;
-  int dt, swz;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  int rank, dt, swz;
   bool operator==(const MapKey& o) const {
-    return base == o.base && inner == o.inner && outer == o.outer && pitch == o.pitch &&
-           box_inner == o.box_inner && box_outer == o.box_outer && dt == o.dt && swz == o.swz;
+    return base == o.base && rank == o.rank && dt == o.dt && swz == o.swz &&
+           std::memcmp(dims, o.dims, sizeof(dims)) == 0 &&
+           std::memcmp(strides, o.strides, sizeof(strides)) == 0 &&
+           std::memcmp(box, o.box, sizeof(box)) == 0;
   }
 };
 constexpr int kMapCacheSize = 64;
@@ -85,11 +86,18 @@ MapCache& map_cache() {
   return c;
 }
 
-bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                 uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
-                 CUtensorMapSwizzle swz) {
-  const MapKey k{base, inner, outer, pitch, box_inner, box_outer, static_cast<int>(dt),
-                 static_cast<int>(swz)};
+// Tiled tensor map of rank 2 or 3: dims[0] contiguous elements, strides in bytes of dims 1, 2.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
+              const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swz) {
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.rank = rank;
+  k.dt = static_cast<int>(dt);
+  k.swz = static_cast<int>(swz);
+  for (int i = 0; i < rank; ++i) k.dims[i] = dims[i], k.box[i] = box[i];
+  for (int i = 0; i + 1 < rank; ++i) k.strides[i] = strides[i];
   MapCache& c = map_cache();
   {
     std::lock_guard<std::mutex> lock(c.mu);
@@ -101,12 +109,12 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) gd[i] = dims[i], bx[i] = box[i];
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
   std::memset(m, 0, sizeof(*m));
-  if (fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+  if (fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
@@ -115,6 +123,17 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   c.key[slot] = k;
   c.map[slot] = *m;
   return true;
+}
+
+// 2-D tiled tensor map: `inner` contiguous elements per row, `outer` rows, `pitch` bytes
+// between rows.
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swz) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {pitch};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return make_map(m, dt, base, 2, dims, strides, box, swz);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -286,6 +305,7 @@ bool wgrad_maps(mgw::WgradArgs* a, const void* gq, const void* gs, const void* x
                    static_cast<uint64_t>(E) * N, static_cast<uint64_t>(K) * 2, 64, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return false;
+  // Scale atoms of the CTA-pair kernel as rows of 256 bytes (an atom is 2 rows).
   if (pair && (!make_map_2d(&a->tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, 256,
                             static_cast<uint64_t>(N) * (Mcap / 32) / 256, 256, 256, 2,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
