@@ -388,14 +388,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_wgrad_kernel(const __grid
 // 128r .. 128r+127 of the B operand; the even CTA issues one
 // tcgen05.mma.cta_group::2.kind::mxf8f6f4 (M=256, N=256, K=32) per 32-token block, which
 // reads A from each CTA's shared memory and B from both halves.  Per 128-token chunk each
-// SM then takes in 32 KB by TMA and reads 8 KB per MMA from its shared memory, against
-// 48 KB and 12 KB for the single-SM tile of the same work per SM: the single-SM kernel's
-// TMA writes plus tensor-core reads exceed what one SM's shared memory serves at the full
-// MMA rate, the pair's stay within it.  The smaller stages also make the ring six deep.
+// SM takes in 32 KB of operands by TMA instead of the single-SM tile's 48 KB for the same
+// work per SM, which leaves room for a six-stage ring.
 //
-// Both CTAs' TMA loads count on the even CTA's full barriers; the even CTA's commits are
-// multicast to both CTAs' empty / accumulator-full barriers; both epilogues release the
-// even CTA's accumulator-empty barrier.  Each CTA's producer ends by waiting until every
+// Scale factors reach TMEM through four writer warps per CTA (one per TMEM lane quarter)
+// with tcgen05.st, not through tcgen05.cp from the MMA-issuing thread: measured on GB300,
+// the three copies per chunk cost that thread ~130 cycles per chunk in which the MMA pipe
+// idles, and a burst of them per window costs the same per copy.  Each CTA's scale atoms
+// land in its own stage slot (bulk copies counted on a local barrier); its writers place
+// them in the stage's TMEM slot and report to the even CTA's sf_ready barrier.
+//
+// Roles (480 threads per CTA):
+//   warp 0       TMA producer (both CTAs): its g^T rows and half of x^T per chunk, counted
+//                on the even CTA's full barrier; its scale atoms on its own sf_full.
+//   warp 1       MMA issuer (even CTA): per chunk waits full and sf_ready, issues four
+//                pair MMAs, commits the stage back to both producers.
+//   warps 2-9    epilogue (both CTAs): drain this CTA's accumulator, release it to the even
+//                CTA, round to bf16, TMA-store 128 x 256 through one staging box.
+//   warp 10      zero writer: this CTA's rows of the tiles of experts without tokens.
+//   warps 11-14  scale writers (both CTAs): one TMEM lane quarter each.
+//
+// Barriers: the even CTA's commits are multicast to both CTAs' empty / accumulator-full
+// barriers; both CTAs' epilogues and scale writers arrive on the even CTA's
+// accumulator-empty and sf_ready barriers.  Each CTA's producer ends by waiting until every
 // stage it filled has been released, so no copy is still landing when a CTA exits.
 constexpr int kPStages = 6;
 constexpr int kPABytes = 128 * BT;                  // 16 KB: this CTA's 128 rows of g^T
@@ -404,9 +419,12 @@ constexpr int kPStageBytes = kPABytes + kPBBytes;   // 32 KB
 constexpr int kPOffOut = kPStages * kPStageBytes;
 constexpr int kPOffSf = kPOffOut + kOutBytes;
 constexpr int kPOffBar = kPOffSf + kPStages * kSfStage;
-constexpr int kPNumBars = 2 * kPStages + 3;        // full[], empty[], acc_full, acc_empty, done
+// full[], empty[], sf_full[], sf_ready[], acc_full, acc_empty, done
+constexpr int kPNumBars = 4 * kPStages + 3;
 constexpr int kPOffMisc = (kPOffBar + kPNumBars * 8 + 15) & ~15;
 constexpr int kPOffTable = kPOffMisc + 16;
+constexpr int kSfWarp0 = 11;                        // scale writers: warps 11-14
+constexpr int kPThreads = (kSfWarp0 + 4) * 32;      // 480
 
 __host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
   return static_cast<size_t>(kPOffTable) + sizeof(int) * (2 * static_cast<size_t>(E) + 2) +
@@ -426,7 +444,31 @@ __device__ __forceinline__ void mma_mxf8_chunk128_pair(uint32_t d, uint64_t ades
   mma_mxf8_block32_pair(d, adesc + 6, bdesc + 6, idesc_mxf8_e4m3(256, 256, 3, 3), sfa, sfb, 1u);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                             uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr)
+               : "memory");
+}
+// 32 lanes x 4 / 8 consecutive 32-bit columns from registers: thread i -> lane (base+i).
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b,
+                                                  uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     grouped_wgrad_pair_kernel(const __grid_constant__ WgradArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -447,7 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Both CTAs read the same offsets, so both return here or neither does.
   if (!load_offsets(args.expert_off, E, args.M, s_off, s_pad, &s_misc[2], args.status)) return;
 
-  for (int e = tid; e < E; e += kThreads) {
+  for (int e = tid; e < E; e += kPThreads) {
     const int ce = s_off[e + 1] - s_off[e];
     int rank_e = 0;
     for (int j = 0; j < E; ++j) {
@@ -457,15 +499,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s_order[rank_e] = static_cast<uint16_t>(e);
   }
   const uint32_t bar0 = sbase + kPOffBar;
-  auto bar_full = [&](int st) { return bar0 + 8u * st; };             // used in the even CTA
+  auto bar_full = [&](int st) { return bar0 + 8u * st; };                   // even CTA
   auto bar_empty = [&](int st) { return bar0 + 8u * (kPStages + st); };
-  const uint32_t bar_acc_full = bar0 + 8u * (2 * kPStages);
-  const uint32_t bar_acc_empty = bar0 + 8u * (2 * kPStages + 1);     // used in the even CTA
-  const uint32_t bar_done = bar0 + 8u * (2 * kPStages + 2);
+  auto bar_sf_full = [&](int st) { return bar0 + 8u * (2 * kPStages + st); };
+  auto bar_sf_ready = [&](int st) { return bar0 + 8u * (3 * kPStages + st); };  // even CTA
+  const uint32_t bar_acc_full = bar0 + 8u * (4 * kPStages);
+  const uint32_t bar_acc_empty = bar0 + 8u * (4 * kPStages + 1);           // even CTA
+  const uint32_t bar_done = bar0 + 8u * (4 * kPStages + 2);
   if (tid == 0) {
     for (int st = 0; st < kPStages; ++st) {
       mbar_init(bar_full(st), 1);
       mbar_init(bar_empty(st), 1);
+      mbar_init(bar_sf_full(st), 1);
+      mbar_init(bar_sf_ready(st), 8);  // four writer warps in each CTA
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, 2 * kEpiWarps);
@@ -473,8 +519,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&args.tm_a);
     tma_prefetch_desc(&args.tm_b);
-    tma_prefetch_desc(&args.tm_sfa);
-    tma_prefetch_desc(&args.tm_sfb);
     tma_prefetch_desc(&args.tm_out);
   }
   if (warp == 1) {
@@ -527,17 +571,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (kPStageBytes + kSfStage));
+          if (leader) mbar_arrive_expect_tx(bar_full(stage), 2 * kPStageBytes);
           const uint32_t fb = full0_leader + 8u * stage;  // the even CTA's full barrier
           const uint32_t sa = sbase + stage * kPStageBytes;
           const int ch = ch0 + c;
           tma_load_2d_pair(sa, &args.tm_a, ch * BT, arow, fb);
           tma_load_2d_pair(sa + kPABytes, &args.tm_b, ch * BT, brow, fb);
-          // scale atoms as rows of 256 bytes (an atom is 2 rows): this CTA's g atom and
-          // both x atoms of the K tile (every CTA's accumulator spans all 256 columns)
+          // this CTA's g atom and both x atoms of the K tile (every CTA's accumulator spans
+          // all 256 columns), counted on this CTA's own sf_full barrier
+          const uint32_t sfb = bar_sf_full(stage);
+          mbar_arrive_expect_tx(sfb, kSfStage);
           const uint32_t ssf = sbase + kPOffSf + stage * kSfStage;
-          tma_load_2d_pair(ssf, &args.tm_sfa, 0, 2 * (ch * (N / 128) + arow / 128), fb);
-          tma_load_2d_pair(ssf + 512, &args.tm_sfb, 0, 2 * (ch * (K / 128) + 2 * kt), fb);
+          bulk_load(ssf, args.gs + (static_cast<size_t>(ch) * (N / 128) + arow / 128) * 512, 512, sfb);
+          bulk_load(ssf + 512, args.xs + (static_cast<size_t>(ch) * (K / 128) + 2 * kt) * 512, 1024, sfb);
           filled[stage] = 1;
           filled_phase[stage] = phase;
           if (++stage == kPStages) stage = 0, phase ^= 1u;
@@ -557,19 +603,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       constexpr uint16_t kBoth = 0x3;
       const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase);
-      const uint64_t sf_desc0 = make_sdesc(sbase + kPOffSf, 0, 128, 0);
-      // Waits for the chunk in `st` to land in both CTAs and copies its scale atoms into
-      // each CTA's TMEM slot (each CTA from its own shared memory).
-      auto stage_scales = [&](int st, uint32_t ph) -> bool {
-        if (!mbar_wait_spin(bar_full(st), ph, abort_flag)) return false;
-        tc_fence_after();
-        const uint64_t dsf = sf_desc0 + static_cast<uint32_t>(st * (kSfStage >> 4));
-        const uint32_t tsf = tmem + kSfCol0 + 16u * st;
-        tmem_cp_32x128b_warpx4_pair(tsf, dsf);
-        tmem_cp_32x128b_warpx4_pair(tsf + 8, dsf + (512 >> 4));
-        tmem_cp_32x128b_warpx4_pair(tsf + 12, dsf + (1024 >> 4));
-        return true;
-      };
       ItemIter items{total, npairs, 0, pair};
       long long it = 0;
       while (ok && items.next(it)) {
@@ -578,13 +611,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (cnt == 0) continue;
         const int nch = (cnt + BT - 1) / BT;
         const int full_chunks = cnt / BT;
-        if (!stage_scales(stage, phase) ||
-            !mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
         for (int c = 0; c < nch; ++c) {
+          // operands in both CTAs, scale factors in both CTAs' TMEM
+          if (!mbar_wait_spin(bar_full(stage), phase, abort_flag) ||
+              !mbar_wait_spin(bar_sf_ready(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const uint32_t tsf = tmem + kSfCol0 + 16u * stage;
           const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (kPStageBytes >> 4));
           const uint64_t bd = ad + (kPABytes >> 4);
@@ -598,10 +636,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           mma_commit_pair(bar_empty(stage), kBoth);
           if (++stage == kPStages) stage = 0, phase ^= 1u;
-          if (c + 1 < nch && !stage_scales(stage, phase)) {
-            ok = false;
-            break;
-          }
         }
         if (!ok) break;
         mma_commit_pair(bar_acc_full, kBoth);
@@ -612,6 +646,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit_pair(bar_done, 0x1);
       mbar_wait_drain(bar_done, 0);
     }
+  } else if (warp >= kSfWarp0) {
+    // ----------------------------------- scale writers: TMEM lane quarter warp % 4
+    // Atom row r0 (16 bytes: words r1 = 0..3, feature r0 + 32 r1, one byte per 32-token
+    // block) goes to TMEM lane r0 of every lane quarter, column r1 of the stage's slot: the
+    // layout tcgen05.mma reads scale factors from (the same bytes a 32x128b.warpx4 copy of
+    // the atom places).
+    const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+    const uint32_t sf_ready0 = map_to_cta(bar_sf_ready(0), 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    ItemIter items{total, npairs, 0, pair};
+    long long it = 0;
+    while (ok && items.next(it)) {
+      const int e = s_order[static_cast<int>(it) / per_expert];
+      const int cnt = s_off[e + 1] - s_off[e];
+      if (cnt == 0) continue;
+      const int nch = (cnt + BT - 1) / BT;
+      for (int c = 0; c < nch; ++c) {
+        if (!mbar_wait(bar_sf_full(stage), phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t ssf = sbase + kPOffSf + stage * kSfStage + 16u * lane;
+        uint32_t a0, a1, a2, a3;
+        uint32_t b[8];
+        ld_shared_v4(ssf, a0, a1, a2, a3);
+        ld_shared_v4(ssf + 512, b[0], b[1], b[2], b[3]);
+        ld_shared_v4(ssf + 1024, b[4], b[5], b[6], b[7]);
+        const uint32_t tsf = tmem + (quarter * 32u << 16) + kSfCol0 + 16u * stage;
+        tmem_st_32x32b_x4(tsf, a0, a1, a2, a3);
+        tmem_st_32x32b_x8(tsf + 8, b);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(sf_ready0 + 8u * stage);
+        if (++stage == kPStages) stage = 0, phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) abort_both();
   } else if (warp == kZeroWarp) {
     // ------------------------ this CTA's rows of the tiles of experts without tokens
     uint8_t* out = static_cast<uint8_t*>(args.out);
@@ -652,18 +726,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!*abort_flag) {
         if (mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
           tc_fence_after();
-          uint32_t r[128];
           const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 128u * half;
-          tmem_ld_32x32b_x32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          tmem_ld_32x32b_x32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-          tmem_ld_32x32b_x32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
-          tmem_wait_ld();
+          // four 32-column quarters, each packed to bf16 as soon as it arrives (keeps the
+          // live registers within the 480-thread budget)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(ta + 32 * h, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[16 * h + j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(acc_empty_leader);
-#pragma unroll
-          for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
         } else if (lane == 0) {
           abort_both();
         }
@@ -727,7 +803,7 @@ cudaError_t launch_grouped_wgrad(const WgradArgs& a, int num_sms, cudaStream_t s
   long long pairs = num_sms / 2;
   if (pairs > total) pairs = total;
   if (pairs < 1) pairs = 1;
-  grouped_wgrad_pair_kernel<<<static_cast<unsigned>(2 * pairs), kThreads,
+  grouped_wgrad_pair_kernel<<<static_cast<unsigned>(2 * pairs), kPThreads,
                               wgrad_pair_smem_bytes(a.E), stream>>>(a);
   return cudaGetLastError();
 }
