@@ -103,6 +103,26 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int c0, int c
       "r"(c0), "r"(c1), "r"(src)
       : "memory");
 }
+// L2 policy that marks lines for eviction first: for output streams written once and not
+// read again, so they leave L2 ahead of the operand tiles that other CTAs still read.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, int c0, int c1, uint32_t src,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(src), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void st_global_zero16_hint(void* p, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %1, %1, %1}, %2;" ::"l"(p), "r"(0u),
+               "l"(policy)
+               : "memory");
+}
 // Contiguous global -> shared bulk copy (16 B aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {

@@ -690,6 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // ------------------------ this CTA's rows of the tiles of experts without tokens
     uint8_t* out = static_cast<uint8_t*>(args.out);
     const size_t pitch = static_cast<size_t>(K) * 2;
+    const uint64_t zpol = l2_policy_evict_first();
     ItemIter items{total, npairs, 0, pair};
     long long it = 0;
     while (items.next(it)) {
@@ -700,8 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       uint8_t* base = out + (static_cast<size_t>(e) * N + np * 256 + 128 * rank) * pitch +
                       static_cast<size_t>(kt) * BN * 2 + lane * 16;
 #pragma unroll 4
-      for (int r = 0; r < BM; ++r)
-        *reinterpret_cast<uint4*>(base + r * pitch) = make_uint4(0u, 0u, 0u, 0u);
+      for (int r = 0; r < BM; ++r) st_global_zero16_hint(base + r * pitch, zpol);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -711,6 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int row = quarter * 32 + static_cast<int>(lane);
     const bool store_leader = (ew == 0 && lane == 0);
     const uint32_t acc_empty_leader = map_to_cta(bar_acc_empty, 0);
+    const uint64_t opol = l2_policy_evict_first();  // grad_w is written once, never re-read here
     uint32_t acc_phase = 0;
     ItemIter items{total, npairs, 0, pair};
     long long it = 0;
@@ -762,7 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
         named_bar_sync(1, kEpiWarps * 32);
         if (store_leader && !*abort_flag) {
-          tma_store_2d(&args.tm_out, kt * BN + 64 * b, orow, stage_base);
+          tma_store_2d_hint(&args.tm_out, kt * BN + 64 * b, orow, stage_base, opol);
           bulk_commit();
         }
       }
