@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libmgw.so")
 # the device time-limit test make a pipeline stage that never fills (MGW_TEST_DROP_LOAD=1).
 # libmgw.so itself has no such switch.
 LIB_TESTHOOKS = os.path.join(HERE, "libmgw_testhooks.so")
-SOURCES = ["api.cu", "quantize.cu", "quantize_rows.cu", "wgrad.cu", "wgrad_balanced.cu", "wgrad_noalloc.cu", "grouped_mm.cu", "dgrad.cu"]
+SOURCES = ["api.cu", "quantize.cu", "quantize_rows.cu", "wgrad.cu", "wgrad_balanced.cu", "wgrad_noalloc.cu", "grouped_mm.cu", "dgrad.cu", "dgrad_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -428,10 +428,6 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
   if (st != MGW_OK) return st;
   mgw::DgradArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!make_map_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W, in_f,
-                   static_cast<uint64_t>(E) * out_f, static_cast<uint64_t>(in_f) * 4, 256, 32,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-    return MGW_ERR_CUDA;
   a.dy = dy;
   a.W = W;
   a.expert_off = expert_off;
@@ -441,7 +437,15 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
   a.out_f = out_f;
   a.in_f = in_f;
   a.status = status_dev;
-  const cudaError_t err = mgw::launch_grouped_dgrad(a, dev.sms, static_cast<cudaStream_t>(stream));
+  // CTA pairs load 128 of a pair tile's 256 columns of W per CTA; the single-SM kernel 256
+  const bool pair = mgw::dgrad_uses_pair(a, dev.sms);
+  if (!make_map_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W, in_f,
+                   static_cast<uint64_t>(E) * out_f, static_cast<uint64_t>(in_f) * 4,
+                   pair ? 128 : 256, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MGW_ERR_CUDA;
+  const cudaError_t err =
+      pair ? mgw::launch_grouped_dgrad_pair(a, dev.sms, static_cast<cudaStream_t>(stream))
+           : mgw::launch_grouped_dgrad(a, dev.sms, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MGW_OK : MGW_ERR_CUDA;
 }
 

@@ -114,4 +114,9 @@ struct DgradArgs {
 };
 cudaError_t launch_grouped_dgrad(const DgradArgs& a, int num_sms, cudaStream_t stream);
 
+// CTA-pair dgrad (dgrad_pair.cu): pair tiles of 256 rows x 256 columns, for problems with
+// enough of them to keep the SM pairs busy; tm_w's box is then 128 columns x 32 rows.
+bool dgrad_uses_pair(const DgradArgs& a, int num_sms);
+cudaError_t launch_grouped_dgrad_pair(const DgradArgs& a, int num_sms, cudaStream_t stream);
+
 }  // namespace mgw

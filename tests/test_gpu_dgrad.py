@@ -102,3 +102,14 @@ def test_dgrad_max_experts():
     dx = _gpu_dgrad(case).cpu().numpy().astype(np.float64)
     ref, bound = oracle.grouped_dgrad(case.dy, case.W, case.expert_off)
     assert np.all(np.abs(dx - ref) <= 1e-5 * bound)
+
+
+def test_dgrad_wide_pair_tiles_ragged():
+    """8192 rows, 64 -> 4096 features, 8 ragged experts (one empty, one of 3 rows): enough
+    work for the 256-column pair tiles; every element against the loop oracle."""
+    counts = [3, 2000, 0, 1500, 777, 1, 2400, 1511]
+    case = synth.dgrad_random(sum(counts), 64, 4096, counts, seed=35)
+    dx = _gpu_dgrad(case).cpu().numpy().astype(np.float64)
+    ref, bound = oracle_dgrad_threads(case.dy, case.W, case.expert_off)
+    bad = np.argwhere(~(np.abs(dx - ref) <= 1e-5 * bound))
+    assert bad.size == 0, (len(bad), bad[:5].tolist())
