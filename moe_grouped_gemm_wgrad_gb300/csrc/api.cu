@@ -437,11 +437,18 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
   a.out_f = out_f;
   a.in_f = in_f;
   a.status = status_dev;
+  a.dx_align32 = (reinterpret_cast<uintptr_t>(dx) & 31) == 0;
   // CTA pairs load 128 of a pair tile's 256 columns of W per CTA; the single-SM kernel 256
   const bool pair = mgw::dgrad_uses_pair(a, dev.sms);
   if (!make_map_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W, in_f,
                    static_cast<uint64_t>(E) * out_f, static_cast<uint64_t>(in_f) * 4,
                    pair ? 128 : 256, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MGW_ERR_CUDA;
+  // dy rows by TMA for the single-SM kernel, 128 rows x 32 columns per chunk (with no row
+  // there is no dy, and the map, which the kernel then never reads, is made over W)
+  if (!pair && !make_map_2d(&a.tm_dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rows > 0 ? dy : W, out_f,
+                            rows > 0 ? static_cast<uint64_t>(rows) : 1,
+                            static_cast<uint64_t>(out_f) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return MGW_ERR_CUDA;
   const cudaError_t err =
       pair ? mgw::launch_grouped_dgrad_pair(a, dev.sms, static_cast<cudaStream_t>(stream))

@@ -1,37 +1,44 @@
-// Grouped fp32 data gradient with 3xTF32 tcgen05 MMAs.
+// Grouped fp32 data gradient with 3xTF32 tcgen05 MMAs, one SM per output tile.
 //
 //   dx[r, k] = sum_n dy[r, n] * W[e(r), n, k],  e(r): the expert whose row range holds r.
 //
 // Work item = (expert e, 128-row tile inside e's row range, 256-column k tile).
 // Tiles start at expert_off[e], so a tile never mixes experts: rows of the tile
-// past the expert's last row are loaded as zero and never stored.  This replaces
+// past the expert's last row hold whatever dy holds there (zeros past the last row),
+// give accumulator rows that are never stored, and change no stored row.  This replaces
 // the dgrad page's split between a tiled path and a per-element path for tiles
 // that straddle an expert boundary.
 //
-// Precision: each fp32 operand x is split as hi = tf32(x), lo = tf32(x - hi)
-// (both rounded with cvt.rna.tf32), and the product is hi*hi + hi*lo + lo*hi
+// Precision: each fp32 operand x is split as hi = tf32(x), lo = x - hi
+// (tf32_split), and the product is hi*hi + hi*lo + lo*hi
 // accumulated in fp32 in TMEM (Ootomo & Yokota, "Recovering single precision
 // accuracy from Tensor Cores while surpassing the FP32 theoretical peak
 // performance", IJHPCA 2022).
 //
 // Data path per 32-wide reduction chunk:
-//   * W[e] rows n (32 of them, 256 k columns) arrive raw by TMA into a two-stage ring;
-//   * the transform warps split them into hi/lo and write the MMA's B operand transposed
-//     (K-major, 128B-swizzled) into a two-stage shared-memory ring, and split the chunk's
-//     dy rows (loaded straight into registers) into hi/lo A operands that they store into
-//     TMEM with tcgen05.st, so A never occupies shared memory;
-//   * the MMA thread issues 4 K-steps x 3 tcgen05.mma.kind::tf32 (M=128, N=256, K=8)
-//     with A from TMEM and B from shared memory into one 256-column accumulator.
+//   * TMA brings W[e] rows n (32 of them, 256 k columns, 32 KB) and the tile's dy rows
+//     (128 rows x 32 n, 16 KB, 128B-swizzled) into a two-stage raw ring;
+//   * per 16-wide half of the chunk, the transform warps read W column-wise, split it and
+//     write the MMA's B operand transposed (K-major, 128B-swizzled, hi in the first and lo
+//     in the second 64 bytes of each row) into a three-stage ring, and read dy row-wise,
+//     split it and store the hi/lo A operands into TMEM with tcgen05.st;
+//   * the MMA thread issues 2 K-steps x 3 tcgen05.mma.kind::tf32 (M=128, N=256, K=8) per
+//     half, A from TMEM and B from shared memory, into one 256-column accumulator.
+// Every shared-memory access of the transform is conflict-free and every global read goes
+// through TMA: per 16-wide half the L1 data pipe moves about 450 wavefronts against 768
+// MMA cycles.  (Reading W and dy with per-thread global loads, or dy rows one per lane,
+// made that pipe the bound at ~2150 wavefronts per 32-wide chunk.)
 //
-// Roles (704 threads):
+// Roles (672 threads):
 //   warps 0-3   epilogue: TMEM lane quarter = warp, 32-column chunks -> fp32 stores of
 //               the rows that belong to the item's expert, then the accumulator is free.
-//   warp 4      MMA issuer.
-//   warps 5-20  transform: per chunk, thread t splits half of B row t % 256 (16 of the 32
-//               reduction elements) and 8 A elements of one row (four warps per TMEM lane
-//               quarter, 8 columns each).  Sixteen warps instead of eight halve each warp's
-//               serial chain of loads, splits and stores per chunk.
-//   warp 21     TMA producer of the raw W tiles.
+//               Lane 0 of warp 0 issues each item's MMAs before its share of the epilogue:
+//               with one accumulator the next item's MMAs wait for the epilogue anyway.
+//   warps 4-19  transform: per half chunk, thread t writes 8 reduction elements of B row
+//               t % 256 and splits 4 A elements of one row (four warps per TMEM lane
+//               quarter, 4 columns each).
+//   warp 20     TMA producer of the raw W and dy tiles, which also prefetches the next eight
+//               chunks of both into L2.
 #include <cstdint>
 
 #include "common.cuh"
@@ -40,48 +47,54 @@
 namespace mgw {
 namespace {
 
-constexpr int BM = 128;  // rows per tile (MMA M)
-constexpr int BN = 256;  // dx columns per tile (MMA N)
-constexpr int BK = 32;   // reduction (out_features) per stage: one 128-byte row of fp32
-constexpr int kStages = 2;
+constexpr int BM = 128;   // rows per tile (MMA M)
+constexpr int BN = 256;   // dx columns per tile (MMA N)
+constexpr int BK = 32;    // reduction (out_features) per raw chunk: one 128-byte row of fp32
+constexpr int BKH = 16;   // reduction per operand stage (half a chunk)
+constexpr int kStages = 3;
 constexpr int kRawStages = 2;
-constexpr int kBTile = BN * BK * 4;             // 32 KB (hi or lo)
-constexpr int kStageBytes = 2 * kBTile;         // B_hi, B_lo = 64 KB
-constexpr int kRawBytes = BK * BN * 4;          // raw W rows: 32 x 256 fp32 = 32 KB
-constexpr int kOffRaw = kStages * kStageBytes;  // 128 KB
-constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
+constexpr int kPrefetch = 8;    // chunks of W and dy prefetched into L2 ahead of the TMA loads
+constexpr int kStageBytes = BN * 128;           // 256 B rows of 16 hi | 16 lo tf32: 32 KB
+constexpr int kRawW = BK * BN * 4;              // raw W rows: 32 x 256 fp32 = 32 KB
+constexpr int kRawDy = BM * BK * 4;             // raw dy rows: 128 x 32 fp32 = 16 KB
+constexpr int kRawBytes = kRawW + kRawDy;
+constexpr int kOffRaw = kStages * kStageBytes;  // 96 KB
+constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;  // 192 KB
 // full[], empty[], raw_full[], raw_empty[], acc_full, acc_empty, done
 constexpr int kNumBars = 2 * kStages + 2 * kRawStages + 3;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kOffMisc = kOffBar + ((kNumBars * 8 + 15) & ~15);
 constexpr int kOffTable = kOffMisc + 16;
 constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kXfWarp0 = 5;
+constexpr int kXfWarp0 = 4;
 constexpr int kXfWarps = 16;
 constexpr int kXfThreads = kXfWarps * 32;
-constexpr int kBParts = kXfThreads / BN;     // threads per B row
-constexpr int kNgPer = (BK / 4) / kBParts;   // groups of 4 reduction elements per thread
-constexpr int kACols = BK / (kXfWarps / 4);  // A columns per transform warp
 constexpr int kTmaWarp = kXfWarp0 + kXfWarps;
 constexpr int kThreads = (kTmaWarp + 1) * 32;
-static_assert(kXfThreads % BN == 0 && (BK / 4) % kBParts == 0 && kACols == 8, "transform split");
+constexpr int kBN = BKH / (kXfThreads / BN);     // B elements per thread and half chunk: 8
+constexpr int kACols = BKH / (kXfWarps / 4);     // A columns per transform warp: 4
+static_assert(kBN == 8 && kACols == 4, "transform split");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol0 = 256;  // A operand slots: stage s hi at 256 + 64s, lo at +32
+constexpr uint32_t kACol0 = 256;  // A operand slots: stage s hi at 256 + 32s, lo at +16
+static_assert(kACol0 + 32 * kStages <= kTmemCols, "TMEM budget");
 
 __host__ __device__ constexpr size_t dgrad_smem_bytes(int E) {
   return static_cast<size_t>(kOffTable) + sizeof(int) * (3 * static_cast<size_t>(E) + 3) + 1024;
 }
 static_assert(dgrad_smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
 
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
-__device__ __forceinline__ void split1(float v, uint32_t& hi, uint32_t& lo) {
-  hi = tf32_rna(v);
-  lo = tf32_rna(v - __uint_as_float(hi));
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -91,11 +104,10 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() {
@@ -115,6 +127,12 @@ __device__ __forceinline__ void mma_tf32_at(uint32_t d, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   int never = 0;
   (void)mbar_wait(bar, parity, &never);
+}
+
+__device__ __forceinline__ void st_global_v8(float* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // Item it -> (expert, row tile in expert, k tile) via the prefix of row-tile counts.
@@ -152,11 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
   const int warp = tid >> 5;
   const uint32_t lane = lane_id();
 
-  if (tid == 0) s_misc[1] = 0;
-  if (!load_offsets(args.expert_off, E, args.rows, s_off, s_pad, &s_misc[2], args.status)) return;
-  // Row tiles per expert = P-scan / 128 (the padded starts count ceil128 rows).
-  for (int e = tid; e <= E; e += kThreads) s_rtp[e] = s_pad[e] / BM;
-
   const uint32_t bar0 = sbase + kOffBar;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
   auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -165,7 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
   const uint32_t bar_acc_full = bar0 + 8u * (2 * kStages + 2 * kRawStages);
   const uint32_t bar_acc_empty = bar_acc_full + 8u;
   const uint32_t bar_done = bar_acc_full + 16u;
+  // Barriers, TMEM and the tensor maps are set up while the offsets are read (after an L2
+  // flush that read is a DRAM round trip).
   if (tid == 0) {
+    s_misc[1] = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full(s), kXfWarps);
       mbar_init(bar_empty(s), 1);
@@ -179,22 +195,30 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
     mbar_init(bar_done, 1);
     fence_mbar_init();
     tma_prefetch_desc(&args.tm_w);
+    tma_prefetch_desc(&args.tm_dy);
   }
-  if (warp == kMmaWarp) {
+  if (warp == 0) {
     tmem_alloc(smem_u32(&s_misc[0]), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  const bool offsets_ok = load_offsets(args.expert_off, E, args.rows, s_off, s_pad, &s_misc[2], args.status);
+  tc_fence_after();  // load_offsets ends with a block barrier
   const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
+  if (!offsets_ok) {
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  // Row tiles per expert = P-scan / 128 (the padded starts count ceil128 rows).
+  for (int e = tid; e <= E; e += kThreads) s_rtp[e] = s_pad[e] / BM;
+  __syncthreads();
 
   const int tiles_k = in_f / BN;
   const long long total = static_cast<long long>(s_rtp[E]) * tiles_k;
   const int nchunks = out_f / BK;
 
   if (warp == kTmaWarp) {
-    // ------------------------------------------------------- raw W tiles by TMA
+    // ---------------------------------------------- raw W and dy tiles by TMA
     if (lane == 0) {
       int rs = 0;
       uint32_t rph = 0;
@@ -202,17 +226,43 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       uint32_t pending_phase[kRawStages];
       for (int s = 0; s < kRawStages; ++s) pending[s] = 0, pending_phase[s] = 0;
       bool ok = true;
+      // L2 prefetch cursor over this CTA's (item, chunk) sequence, kPrefetch chunks ahead of
+      // the loads: the two-stage ring alone leaves each load a DRAM round trip to hide.
+      long long pf_it = blockIdx.x;
+      int pf_c = 0, pf_row0 = 0;
+      Item pf_item{0, 0, 0};
+      auto pf_set = [&]() {
+        if (pf_it < total) {
+          pf_item = decode_item(pf_it, tiles_k, s_rtp, E);
+          pf_row0 = s_off[pf_item.e] + pf_item.rt * BM;
+        }
+      };
+      auto prefetch_next = [&]() {
+        if (pf_it >= total) return;
+        tma_prefetch_l2_2d(&args.tm_w, pf_item.kt * BN, pf_item.e * out_f + pf_c * BK);
+        tma_prefetch_l2_2d(&args.tm_dy, pf_c * BK, pf_row0);
+        if (++pf_c == nchunks) {
+          pf_c = 0;
+          pf_it += gridDim.x;
+          pf_set();
+        }
+      };
+      pf_set();
+      for (int i = 0; i < kPrefetch; ++i) prefetch_next();
       for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item item = decode_item(it, tiles_k, s_rtp, E);
+        const int row0 = s_off[item.e] + item.rt * BM;
         for (int c = 0; c < nchunks; ++c) {
           if (!mbar_wait(bar_raw_empty(rs), rph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar_raw_full(rs);
+          const uint32_t dst = sbase + kOffRaw + rs * kRawBytes;
           mbar_arrive_expect_tx(fb, kRawBytes);
-          tma_load_2d(sbase + kOffRaw + rs * kRawBytes, &args.tm_w, item.kt * BN,
-                      item.e * out_f + c * BK, fb);
+          tma_load_2d(dst, &args.tm_w, item.kt * BN, item.e * out_f + c * BK, fb);
+          tma_load_2d(dst + kRawW, &args.tm_dy, c * BK, row0, fb);
+          prefetch_next();
           pending[rs] = 1;
           pending_phase[rs] = rph;
           if (++rs == kRawStages) rs = 0, rph ^= 1u;
@@ -230,125 +280,124 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
     const int xw = warp - kXfWarp0;              // 0..15
     const int xt = tid - kXfWarp0 * 32;          // 0..511
     const int bk = xt % BN;                      // the B row k of this thread
-    const int ng0 = (xt / BN) * kNgPer;          // its first group of 4 reduction elements
+    const int part = xt / BN;                    // its 8 of the half chunk's 16 n
     const uint32_t q = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter for A
-    const int kh = xw >> 2;                      // A columns 8*kh .. 8*kh+7 of the chunk
+    const int kh = xw >> 2;                      // A columns 4*kh .. 4*kh+3 of a half chunk
+    const int r = static_cast<int>(q) * 32 + static_cast<int>(lane);  // this thread's A row
+    const uint32_t sw_b = static_cast<uint32_t>(bk & 7);  // 128B swizzle of B row bk
+    const uint32_t sw_a = static_cast<uint32_t>(r & 7);   // and of dy row r
     int stage = 0, rs = 0;
     uint32_t phase = 0, rph = 0;
     bool ok = true;
     for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const Item item = decode_item(it, tiles_k, s_rtp, E);
-      const int row0 = s_off[item.e] + item.rt * BM;
-      const int valid = min(BM, s_off[item.e + 1] - row0);
-      const int r = static_cast<int>(q) * 32 + static_cast<int>(lane);  // this thread's A row
-      const float* dyrow = args.dy + static_cast<size_t>(row0 + (r < valid ? r : 0)) * out_f + kACols * kh;
       for (int c = 0; c < nchunks; ++c) {
-        // A: 8 consecutive reduction elements of row r, straight from global memory
-        float4 a4[kACols / 4];
-#pragma unroll
-        for (int j = 0; j < kACols / 4; ++j) {
-          a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (r < valid) a4[j] = __ldg(reinterpret_cast<const float4*>(dyrow + c * BK) + j);
-        }
-        if (!mbar_wait(bar_raw_full(rs), rph, abort_flag) ||
-            !mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(bar_raw_full(rs), rph, abort_flag)) {
           ok = false;
           break;
         }
-        // B: row k = bk of the K-major tile holds W[n][k] for the chunk's 32 n; this thread
-        // reads its half of column k of the raw [32 n][256 k] tile (conflict-free) and writes
-        // 4 x 16 bytes of each of the hi and lo rows
-        const float* raw = reinterpret_cast<const float*>(smem + kOffRaw + rs * kRawBytes);
-        const uint32_t s_bhi = sbase + stage * kStageBytes;
-        const uint32_t s_blo = s_bhi + kBTile;
+        const uint32_t raw_w = sbase + kOffRaw + rs * kRawBytes;
+        const uint32_t raw_dy = raw_w + kRawW;
 #pragma unroll
-        for (int g = 0; g < kNgPer; ++g) {
-          const int ng = ng0 + g;
-          uint32_t h[4], l[4];
+        for (int h = 0; h < 2; ++h) {
+          // W[n][k] for n = 16h + 8part + j of the chunk: column bk of the raw [32 n][256 k]
+          // tile (a warp reads 32 consecutive k: conflict-free)
+          float w[kBN];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) split1(raw[(4 * ng + j) * BN + bk], h[j], l[j]);
-          const uint32_t off = bk * 128 + ((ng ^ (bk & 7)) << 4);
-          st_shared_u4(s_bhi + off, h[0], h[1], h[2], h[3]);
-          st_shared_u4(s_blo + off, l[0], l[1], l[2], l[3]);
+          for (int j = 0; j < kBN; ++j)
+            w[j] = ld_shared_f32(raw_w + static_cast<uint32_t>(((BKH * h + kBN * part + j) * BN + bk) * 4));
+          // dy[r][16h + 4kh .. +3]: 16-byte chunk 4h + kh of row r (a warp reads 32 rows at one
+          // logical chunk, which the swizzle spreads over all banks)
+          const float4 a = ld_shared_f4(raw_dy + static_cast<uint32_t>(r * 128) +
+                                        (((4u * h + kh) ^ sw_a) << 4));
+          if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // B row bk: hi in 16-byte chunks 0-3, lo in 4-7 (logical), 128B-swizzled
+          {
+            uint32_t hi[kBN], lo[kBN];
+#pragma unroll
+            for (int j = 0; j < kBN; ++j) tf32_split(w[j], hi[j], lo[j]);
+            const uint32_t row = sbase + stage * kStageBytes + bk * 128;
+            const uint32_t c0 = 2u * part;
+            st_shared_u4(row + ((c0 ^ sw_b) << 4), hi[0], hi[1], hi[2], hi[3]);
+            st_shared_u4(row + (((c0 + 1u) ^ sw_b) << 4), hi[4], hi[5], hi[6], hi[7]);
+            st_shared_u4(row + (((c0 + 4u) ^ sw_b) << 4), lo[0], lo[1], lo[2], lo[3]);
+            st_shared_u4(row + (((c0 + 5u) ^ sw_b) << 4), lo[4], lo[5], lo[6], lo[7]);
+          }
+          // A hi/lo into this stage's TMEM slot, this warp's lane quarter and 4-column group
+          {
+            uint32_t ah[4], al[4];
+            tf32_split(a.x, ah[0], al[0]);
+            tf32_split(a.y, ah[1], al[1]);
+            tf32_split(a.z, ah[2], al[2]);
+            tf32_split(a.w, ah[3], al[3]);
+            const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 32u * stage + kACols * kh;
+            tmem_st_x4(ta, ah);
+            tmem_st_x4(ta + 16, al);
+            tmem_wait_st();
+          }
+          fence_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_full(stage));
+          if (++stage == kStages) stage = 0, phase ^= 1u;
         }
+        if (!ok) break;
+        // both halves of the raw stage are read
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_raw_empty(rs));
         if (++rs == kRawStages) rs = 0, rph ^= 1u;
-        // A hi/lo into this stage's TMEM slot, this warp's lane quarter and 8-column group
-        {
-          uint32_t ah[kACols], al[kACols];
-#pragma unroll
-          for (int j = 0; j < kACols / 4; ++j) {
-            split1(a4[j].x, ah[4 * j], al[4 * j]);
-            split1(a4[j].y, ah[4 * j + 1], al[4 * j + 1]);
-            split1(a4[j].z, ah[4 * j + 2], al[4 * j + 2]);
-            split1(a4[j].w, ah[4 * j + 3], al[4 * j + 3]);
-          }
-          const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 64u * stage + kACols * kh;
-          tmem_st_x8(ta, ah);
-          tmem_st_x8(ta + 32, al);
-          tmem_wait_st();
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_full(stage));
-        if (++stage == kStages) stage = 0, phase ^= 1u;
       }
     }
     if (!ok) {
       *abort_flag = 1;
       if (lane == 0 && args.status) atomicOr(args.status, kDevTimeout);
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      constexpr uint32_t idesc = idesc_tf32(BM, BN);
-      const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase);
-      for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
-        if (!mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        acc_phase ^= 1u;
+  } else {
+    // ---------------------------------------- MMA issuer (warp 0, lane 0) and epilogue
+    const int quarter = warp;  // warps 0-3
+    const bool issuer = warp == 0 && lane == 0;
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    constexpr uint32_t idesc = idesc_tf32(BM, BN);
+    const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase);
+    const int nhalves = 2 * nchunks;
+    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+      if (issuer && ok) {
+        // the previous item's epilogue (all four warps) has read the accumulator
+        ok = mbar_wait_spin(bar_acc_empty, acc_phase ^ 1u, abort_flag);
         tc_fence_after();
-        for (int c = 0; c < nchunks; ++c) {
+        for (int hc = 0; hc < nhalves && ok; ++hc) {
           if (!mbar_wait_spin(bar_full(stage), phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          // B row: hi at bytes 0-63 (K-steps at +0, +32), lo at 64-127 (desc units of 16 B)
           const uint64_t bhi = b_desc0 + static_cast<uint32_t>(stage * (kStageBytes >> 4));
-          const uint64_t blo = bhi + (kBTile >> 4);
-          const uint32_t ahi = tmem + kACol0 + 64u * stage;
-          const uint32_t alo = ahi + 32u;
+          const uint64_t blo = bhi + 4;
+          const uint32_t ahi = tmem + kACol0 + 32u * stage;
+          const uint32_t alo = ahi + 16u;
 #pragma unroll
-          for (int ks = 0; ks < BK / 8; ++ks) {
-            mma_tf32_at(tmem, alo + 8u * ks, bhi + 2 * ks, idesc, (c | ks) != 0);
+          for (int ks = 0; ks < BKH / 8; ++ks) {
+            mma_tf32_at(tmem, alo + 8u * ks, bhi + 2 * ks, idesc, (hc | ks) != 0);
             mma_tf32_at(tmem, ahi + 8u * ks, blo + 2 * ks, idesc, 1u);
             mma_tf32_at(tmem, ahi + 8u * ks, bhi + 2 * ks, idesc, 1u);
           }
           mma_commit(bar_empty(stage));
           if (++stage == kStages) stage = 0, phase ^= 1u;
         }
-        if (!ok) break;
-        mma_commit(bar_acc_full);
+        if (ok) {
+          mma_commit(bar_acc_full);
+        } else {
+          *abort_flag = 1;
+          if (args.status) atomicOr(args.status, kDevTimeout);
+        }
       }
-      if (!ok) {
-        *abort_flag = 1;
-        if (args.status) atomicOr(args.status, kDevTimeout);
-      }
-      mma_commit(bar_done);
-      mbar_wait_drain(bar_done, 0);
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int quarter = warp;  // warps 0-3
-    uint32_t acc_phase = 0;
-    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+      __syncwarp();
       if (*abort_flag) break;
       if (!mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
         *abort_flag = 1;
@@ -361,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       const int row0 = s_off[item.e] + item.rt * BM;
       const int valid = min(BM, s_off[item.e + 1] - row0);
       const int r = quarter * 32 + static_cast<int>(lane);
-      float* dst = args.dx + static_cast<size_t>(row0 + r) * in_f + item.kt * BN;
+      float* dst = args.dx + static_cast<size_t>(row0 + (r < valid ? r : 0)) * in_f + item.kt * BN;
       const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
       for (int j = 0; j < BN / 32; ++j) {
@@ -369,23 +418,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
         tmem_ld_32x32b_x32(ta + 32u * j, v);
         tmem_wait_ld();
         if (r < valid) {
+          if (args.dx_align32) {
+            // whole 32-byte sectors per store
 #pragma unroll
-          for (int qq = 0; qq < 8; ++qq)
-            *reinterpret_cast<float4*>(dst + 32 * j + 4 * qq) =
-                make_float4(__uint_as_float(v[4 * qq]), __uint_as_float(v[4 * qq + 1]),
-                            __uint_as_float(v[4 * qq + 2]), __uint_as_float(v[4 * qq + 3]));
+            for (int qq = 0; qq < 4; ++qq) st_global_v8(dst + 32 * j + 8 * qq, v + 8 * qq);
+          } else {
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+              *reinterpret_cast<float4*>(dst + 32 * j + 4 * qq) =
+                  make_float4(__uint_as_float(v[4 * qq]), __uint_as_float(v[4 * qq + 1]),
+                              __uint_as_float(v[4 * qq + 2]), __uint_as_float(v[4 * qq + 3]));
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);
     }
+    if (issuer) {
+      mma_commit(bar_done);
+      mbar_wait_drain(bar_done, 0);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace

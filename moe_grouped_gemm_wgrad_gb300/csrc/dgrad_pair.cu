@@ -3,7 +3,7 @@
 //   dx[r, k] = sum_n dy[r, n] * W[e(r), n, k],  e(r): the expert whose row range holds r.
 //
 // The same product and splits as grouped_dgrad_kernel (dgrad.cu): each fp32 operand x is
-// split as hi = tf32(x), lo = tf32(x - hi) (cvt.rna.tf32) and the product is
+// split as hi = tf32(x), lo = x - hi (tf32_split) and the product is
 // hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM (Ootomo & Yokota, "Recovering single
 // precision accuracy from Tensor Cores while surpassing the FP32 theoretical peak
 // performance", IJHPCA 2022).
@@ -79,15 +79,6 @@ struct Layout {
 constexpr int kPairN = 256;  // the pair tile's columns (each CTA holds 128 of them)
 static_assert(Layout<kPairN>::smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
 
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void split1(float v, uint32_t& hi, uint32_t& lo) {
-  hi = tf32_rna(v);
-  lo = tf32_rna(v - __uint_as_float(hi));
-}
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -303,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int ng = ng0 + g;
           uint32_t h[4], l[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) split1(raw[(4 * ng + j) * L::kHalf + bk], h[j], l[j]);
+          for (int j = 0; j < 4; ++j) tf32_split(raw[(4 * ng + j) * L::kHalf + bk], h[j], l[j]);
           const uint32_t off = bk * 128 + ((ng ^ (bk & 7)) << 4);
           st_shared_u4(s_bhi + off, h[0], h[1], h[2], h[3]);
           st_shared_u4(s_blo + off, l[0], l[1], l[2], l[3]);
@@ -316,10 +307,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t ah[kACols], al[kACols];
 #pragma unroll
           for (int j = 0; j < kACols / 4; ++j) {
-            split1(a4[j].x, ah[4 * j], al[4 * j]);
-            split1(a4[j].y, ah[4 * j + 1], al[4 * j + 1]);
-            split1(a4[j].z, ah[4 * j + 2], al[4 * j + 2]);
-            split1(a4[j].w, ah[4 * j + 3], al[4 * j + 3]);
+            tf32_split(a4[j].x, ah[4 * j], al[4 * j]);
+            tf32_split(a4[j].y, ah[4 * j + 1], al[4 * j + 1]);
+            tf32_split(a4[j].z, ah[4 * j + 2], al[4 * j + 2]);
+            tf32_split(a4[j].w, ah[4 * j + 3], al[4 * j + 3]);
           }
           const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 64u * stage + kACols * kh;
           tmem_st_x8(ta, ah);

@@ -105,12 +105,14 @@ cudaError_t launch_grouped_mm_mxfp8(const MmArgs& a, int num_sms, cudaStream_t s
 
 struct DgradArgs {
   CUtensorMap tm_w;    // W fp32 [E*out_f, in_f], box 256 columns x 32 rows, no swizzle
+  CUtensorMap tm_dy;   // dy fp32 [rows, out_f], box 32 columns x 128 rows, 128B swizzle
   const float* dy;
   const float* W;
   const int32_t* expert_off;
   float* dx;
   int E, rows, out_f, in_f;
   int* status;
+  int dx_align32;      // dx is 32-byte aligned: the epilogue stores whole 32-byte sectors
 };
 cudaError_t launch_grouped_dgrad(const DgradArgs& a, int num_sms, cudaStream_t stream);
 
