@@ -444,11 +444,11 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
                    static_cast<uint64_t>(E) * out_f, static_cast<uint64_t>(in_f) * 4,
                    pair ? 128 : 256, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MGW_ERR_CUDA;
-  // dy rows by TMA for the single-SM kernel, 128 rows x 32 columns per chunk (with no row
-  // there is no dy, and the map, which the kernel then never reads, is made over W)
-  if (!pair && !make_map_2d(&a.tm_dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rows > 0 ? dy : W, out_f,
-                            rows > 0 ? static_cast<uint64_t>(rows) : 1,
-                            static_cast<uint64_t>(out_f) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+  // dy rows by TMA, 128 rows x 32 columns per CTA and chunk (with no row there is no dy, and
+  // the map, which the kernel then never reads, is made over W)
+  if (!make_map_2d(&a.tm_dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rows > 0 ? dy : W, out_f,
+                   rows > 0 ? static_cast<uint64_t>(rows) : 1, static_cast<uint64_t>(out_f) * 4,
+                   32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return MGW_ERR_CUDA;
   const cudaError_t err =
       pair ? mgw::launch_grouped_dgrad_pair(a, dev.sms, static_cast<cudaStream_t>(stream))

@@ -41,22 +41,21 @@
 //               chunks of both into L2.
 #include <cstdint>
 
-#include "common.cuh"
-#include "kernels.h"
+#include "dgrad.cuh"
 
 namespace mgw {
 namespace {
 
+using namespace dgrad;
+
 constexpr int BM = 128;   // rows per tile (MMA M)
 constexpr int BN = 256;   // dx columns per tile (MMA N)
-constexpr int BK = 32;    // reduction (out_features) per raw chunk: one 128-byte row of fp32
-constexpr int BKH = 16;   // reduction per operand stage (half a chunk)
 constexpr int kStages = 3;
 constexpr int kRawStages = 2;
 constexpr int kPrefetch = 8;    // chunks of W and dy prefetched into L2 ahead of the TMA loads
 constexpr int kStageBytes = BN * 128;           // 256 B rows of 16 hi | 16 lo tf32: 32 KB
 constexpr int kRawW = BK * BN * 4;              // raw W rows: 32 x 256 fp32 = 32 KB
-constexpr int kRawDy = BM * BK * 4;             // raw dy rows: 128 x 32 fp32 = 16 KB
+static_assert(BM == kRowsPerCta, "one TMEM lane per row");
 constexpr int kRawBytes = kRawW + kRawDy;
 constexpr int kOffRaw = kStages * kStageBytes;  // 96 KB
 constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;  // 192 KB
@@ -82,38 +81,6 @@ __host__ __device__ constexpr size_t dgrad_smem_bytes(int E) {
 }
 static_assert(dgrad_smem_bytes(kMaxExperts) <= 232448, "shared memory budget");
 
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, const uint32_t (&v)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::tf32 (A: M rows in TMEM lanes, K in columns).
 __device__ __forceinline__ void mma_tf32_at(uint32_t d, uint32_t a_tmem, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -122,38 +89,6 @@ __device__ __forceinline__ void mma_tf32_at(uint32_t d, uint32_t a_tmem, uint64_
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  int never = 0;
-  (void)mbar_wait(bar, parity, &never);
-}
-
-__device__ __forceinline__ void st_global_v8(float* p, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-
-// Item it -> (expert, row tile in expert, k tile) via the prefix of row-tile counts.
-struct Item {
-  int e, rt, kt;
-};
-__device__ __forceinline__ Item decode_item(long long it, int tiles_k, const int* s_rtp, int E) {
-  const int t = static_cast<int>(it / tiles_k);
-  Item r;
-  r.kt = static_cast<int>(it % tiles_k);
-  int lo = 0, hi = E - 1;  // largest e with s_rtp[e] <= t (a non-empty expert)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_rtp[mid] <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  r.e = lo;
-  r.rt = t - s_rtp[lo];
-  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid_constant__ DgradArgs args) {
@@ -237,10 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
           pf_row0 = s_off[pf_item.e] + pf_item.rt * BM;
         }
       };
-      auto prefetch_next = [&]() {
+      auto pf_advance = [&](bool prefetch) {
         if (pf_it >= total) return;
-        tma_prefetch_l2_2d(&args.tm_w, pf_item.kt * BN, pf_item.e * out_f + pf_c * BK);
-        tma_prefetch_l2_2d(&args.tm_dy, pf_c * BK, pf_row0);
+        if (prefetch) {
+          tma_prefetch_l2_2d(&args.tm_w, pf_item.kt * BN, pf_item.e * out_f + pf_c * BK);
+          tma_prefetch_l2_2d(&args.tm_dy, pf_c * BK, pf_row0);
+        }
         if (++pf_c == nchunks) {
           pf_c = 0;
           pf_it += gridDim.x;
@@ -248,7 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
         }
       };
       pf_set();
-      for (int i = 0; i < kPrefetch; ++i) prefetch_next();
+      // The ring's first loads go out before any prefetch (the TMA unit serves them in
+      // order); the cursor then starts past them and catches up two chunks per load.
+      for (int i = 0; i < kRawStages; ++i) pf_advance(false);
+      int ahead = kRawStages;
       for (long long it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item item = decode_item(it, tiles_k, s_rtp, E);
         const int row0 = s_off[item.e] + item.rt * BM;
@@ -262,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
           mbar_arrive_expect_tx(fb, kRawBytes);
           tma_load_2d(dst, &args.tm_w, item.kt * BN, item.e * out_f + c * BK, fb);
           tma_load_2d(dst + kRawW, &args.tm_dy, c * BK, row0, fb);
-          prefetch_next();
+          --ahead;
+          for (int k = 0; k < 2 && ahead < kPrefetch; ++k, ++ahead) pf_advance(true);
           pending[rs] = 1;
           pending_phase[rs] = rph;
           if (++rs == kRawStages) rs = 0, rph ^= 1u;
@@ -283,9 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
     const int part = xt / BN;                    // its 8 of the half chunk's 16 n
     const uint32_t q = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter for A
     const int kh = xw >> 2;                      // A columns 4*kh .. 4*kh+3 of a half chunk
-    const int r = static_cast<int>(q) * 32 + static_cast<int>(lane);  // this thread's A row
     const uint32_t sw_b = static_cast<uint32_t>(bk & 7);  // 128B swizzle of B row bk
-    const uint32_t sw_a = static_cast<uint32_t>(r & 7);   // and of dy row r
     int stage = 0, rs = 0;
     uint32_t phase = 0, rph = 0;
     bool ok = true;
@@ -305,10 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < kBN; ++j)
             w[j] = ld_shared_f32(raw_w + static_cast<uint32_t>(((BKH * h + kBN * part + j) * BN + bk) * 4));
-          // dy[r][16h + 4kh .. +3]: 16-byte chunk 4h + kh of row r (a warp reads 32 rows at one
-          // logical chunk, which the swizzle spreads over all banks)
-          const float4 a = ld_shared_f4(raw_dy + static_cast<uint32_t>(r * 128) +
-                                        (((4u * h + kh) ^ sw_a) << 4));
+          const float4 a = load_a(raw_dy, h, q, lane, kh);
           if (!mbar_wait(bar_empty(stage), phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -327,17 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
             st_shared_u4(row + (((c0 + 5u) ^ sw_b) << 4), lo[4], lo[5], lo[6], lo[7]);
           }
           // A hi/lo into this stage's TMEM slot, this warp's lane quarter and 4-column group
-          {
-            uint32_t ah[4], al[4];
-            tf32_split(a.x, ah[0], al[0]);
-            tf32_split(a.y, ah[1], al[1]);
-            tf32_split(a.z, ah[2], al[2]);
-            tf32_split(a.w, ah[3], al[3]);
-            const uint32_t ta = tmem + (q * 32u << 16) + kACol0 + 32u * stage + kACols * kh;
-            tmem_st_x4(ta, ah);
-            tmem_st_x4(ta + 16, al);
-            tmem_wait_st();
-          }
+          store_a(a, q, kh, tmem, kACol0 + 32u * stage);
+          tmem_wait_st();
           fence_async_smem();
           tc_fence_before();
           __syncwarp();
@@ -409,28 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       const Item item = decode_item(it, tiles_k, s_rtp, E);
       const int row0 = s_off[item.e] + item.rt * BM;
       const int valid = min(BM, s_off[item.e + 1] - row0);
-      const int r = quarter * 32 + static_cast<int>(lane);
-      float* dst = args.dx + static_cast<size_t>(row0 + (r < valid ? r : 0)) * in_f + item.kt * BN;
-      const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-      for (int j = 0; j < BN / 32; ++j) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(ta + 32u * j, v);
-        tmem_wait_ld();
-        if (r < valid) {
-          if (args.dx_align32) {
-            // whole 32-byte sectors per store
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) st_global_v8(dst + 32 * j + 8 * qq, v + 8 * qq);
-          } else {
-#pragma unroll
-            for (int qq = 0; qq < 8; ++qq)
-              *reinterpret_cast<float4*>(dst + 32 * j + 4 * qq) =
-                  make_float4(__uint_as_float(v[4 * qq]), __uint_as_float(v[4 * qq + 1]),
-                              __uint_as_float(v[4 * qq + 2]), __uint_as_float(v[4 * qq + 3]));
-          }
-        }
-      }
+      store_acc_rows(args, tmem, quarter, lane, row0, valid, item.kt * BN, BN);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);
