@@ -49,17 +49,4 @@ __device__ __forceinline__ bool load_offsets(const int32_t* __restrict__ expert_
   return true;
 }
 
-// 3xTF32 operand split (Ootomo & Yokota, "Recovering single precision accuracy from Tensor
-// Cores while surpassing the FP32 theoretical peak performance", IJHPCA 2022): hi is x rounded
-// to tf32 (10 stored mantissa bits), to nearest with ties away from zero, done on the
-// sign-magnitude bits: add half the weight of the 13 dropped bits, then clear them.  lo = x - hi
-// is exact in fp32 (|x - hi| <= 2^-11 |x|, and hi lies within a factor 2 of x), and it is
-// handed to the tensor core as it is: reading it as tf32 drops or rounds its low 13 bits, an
-// error of at most 2^-10 |lo| <= 2^-21 |x|.  Integer and fp32 adds only, no conversion
-// instruction: the conversions' lower throughput bounded the transform warps.
-__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
-  hi = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
-  lo = __float_as_uint(x - __uint_as_float(hi));
-}
-
 }  // namespace mgw

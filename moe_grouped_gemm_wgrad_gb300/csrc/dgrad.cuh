@@ -27,6 +27,26 @@ constexpr int BKH = 16;   // reduction per operand stage (half a chunk)
 constexpr int kRowsPerCta = 128;            // A rows (dx rows) per CTA: the TMEM lanes
 constexpr int kRawDy = kRowsPerCta * BK * 4;  // raw dy rows per CTA and chunk: 16 KB
 
+// 3xTF32 operand split: hi is x rounded to tf32 (10 stored mantissa bits), to nearest with ties
+// away from zero, done on the sign-magnitude bits: add half the weight of the 13 dropped bits,
+// then clear them.  lo = x - hi is exact in fp32 (|x - hi| <= 2^-11 |x|, and hi lies within a
+// factor 2 of x), and it is handed to the tensor core as it is: reading it as tf32 drops or
+// rounds its low 13 bits, an error of at most 2^-10 |lo| <= 2^-21 |x|.  Integer and fp32 adds
+// only, no conversion instruction: the conversions' lower throughput bounded the transform
+// warps.
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  hi = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// Brings a tile of a tensor map into L2 only (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
