@@ -722,7 +722,8 @@ def main():
     ap.add_argument("--workload", default="wgrad_8192",
                     choices=["wgrad_tiny", "wgrad_8192", "wgrad_skew", "moe_ffn_pair"])
     ap.add_argument("--dgrad-workloads", default="dgrad_4096,moe_ffn_pair",
-                    help="comma list of fp32 dgrad legs (dgrad_4096, moe_ffn_pair) or none")
+                    help="comma list of fp32 dgrad legs (dgrad_4096, moe_ffn_pair; moe_ffn_slice, a "
+                         "16-expert slice for profiler captures) or none")
     ap.add_argument("--wgrad-step-workloads", default="wgrad_tiny,moe_ffn_pair",
                     help="comma list of extra whole-step wgrad legs (wgrad_tiny, wgrad_skew, "
                          "moe_ffn_pair) or none")

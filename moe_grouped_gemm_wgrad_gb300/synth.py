@@ -176,4 +176,14 @@ def moe_ffn_pair(seed: int = 0, tokens: int = 8192, E: int = 64, hidden: int = 4
     return wg, dg
 
 
+def moe_ffn_slice(seed: int = 0) -> DgradCase:
+    """A 16-expert slice of the MoE FFN pair's fp32 data gradient (2048 tokens, top-8 of 16
+    experts: 16384 routed rows, ffn 1536 -> hidden 4096, 0.8 GB on the device), small enough
+    for a full profiler capture of the CTA-pair dgrad kernel.  Not one of the workload
+    configurations."""
+    dg = moe_ffn_pair(seed, tokens=2048, E=16)[1]
+    dg.name = "moe_ffn_slice.dgrad"
+    return dg
+
+
 WORKLOADS = ("wgrad_tiny", "dgrad_4096", "wgrad_8192", "wgrad_skew", "moe_ffn_pair")
