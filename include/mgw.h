@@ -51,6 +51,7 @@ typedef int mgw_status;
 #define MGW_DEV_BAD_OFFSETS 1 /* expert_off[0] != 0, decreasing, or expert_off[E] != M/rows */
 #define MGW_DEV_TIMEOUT 2     /* an internal pipeline wait exceeded 1 s; outputs undefined */
 #define MGW_DEV_BAD_INDEX 4   /* mgw_mxfp8_quantize_gather: a row index outside the source */
+#define MGW_DEV_BOUNDS 8      /* diagnostic library only (mgw_diag.h): a computed address outside its tensor */
 
 #define MGW_MAX_EXPERTS 1024
 

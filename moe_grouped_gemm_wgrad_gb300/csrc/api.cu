@@ -9,6 +9,9 @@
 #include <mutex>
 
 #include "../../include/mgw.h"
+#ifdef MGW_DIAG
+#include "../../include/mgw_diag.h"
+#endif
 #include "kernels.h"
 
 namespace {
@@ -321,6 +324,7 @@ bool wgrad_maps(mgw::WgradArgs* a, const void* gq, const void* gs, const void* x
   a->M = M;
   a->N = N;
   a->K = K;
+  a->mcap = static_cast<long long>(Mcap);
   a->status = status_dev;
   return true;
 }
@@ -561,3 +565,36 @@ mgw_status mgw_grouped_dgrad_mxfp8(const void* dyq, const void* dys, const void*
 }
 
 }  // extern "C"
+
+#ifdef MGW_DIAG
+extern "C" {
+
+mgw_status mgw_diag_timeline(mgw_diag_record* out, int cap, int* total) {
+  if (!total || cap < 0 || (cap > 0 && !out)) return MGW_ERR_INVALID_ARG;
+  static_assert(sizeof(mgw_diag_record) == sizeof(mgw::DiagRecord), "record layout");
+  using Read = cudaError_t (*)(mgw::DiagRecord*, int, int*);
+  const Read readers[3] = {mgw::diag_timeline_read_wgrad, mgw::diag_timeline_read_dgrad,
+                           mgw::diag_timeline_read_dgrad_pair};
+  auto* dst = reinterpret_cast<mgw::DiagRecord*>(out);
+  int copied = 0, recorded = 0;
+  for (Read read : readers) {
+    int n = 0;
+    if (read(dst + copied, cap - copied, &n) != cudaSuccess) return MGW_ERR_CUDA;
+    const int kept = n < mgw::kDiagTimelineCap ? n : mgw::kDiagTimelineCap;
+    copied += kept < cap - copied ? kept : cap - copied;
+    recorded += n;
+  }
+  *total = recorded;
+  return MGW_OK;
+}
+
+mgw_status mgw_diag_timeline_reset(void) {
+  if (mgw::diag_timeline_reset_wgrad() != cudaSuccess ||
+      mgw::diag_timeline_reset_dgrad() != cudaSuccess ||
+      mgw::diag_timeline_reset_dgrad_pair() != cudaSuccess)
+    return MGW_ERR_CUDA;
+  return MGW_OK;
+}
+
+}  // extern "C"
+#endif  // MGW_DIAG

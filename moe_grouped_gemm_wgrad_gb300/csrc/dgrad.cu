@@ -44,6 +44,9 @@
 #include "dgrad.cuh"
 
 namespace mgw {
+
+MGW_DIAG_TIMELINE_DEFINE(dgrad, 2)
+
 namespace {
 
 using namespace dgrad;
@@ -200,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
           const uint32_t fb = bar_raw_full(rs);
           const uint32_t dst = sbase + kOffRaw + rs * kRawBytes;
           mbar_arrive_expect_tx(fb, kRawBytes);
+          (void)MGW_DIAG_CHECK(item.e * out_f + (c + 1) * BK <= E * out_f &&
+                                   (item.kt + 1) * BN <= in_f && (c + 1) * BK <= out_f &&
+                                   row0 < args.rows,
+                               args.status);
           tma_load_2d(dst, &args.tm_w, item.kt * BN, item.e * out_f + c * BK, fb);
           tma_load_2d(dst + kRawW, &args.tm_dy, c * BK, row0, fb);
           --ahead;
@@ -326,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       }
       __syncwarp();
       if (*abort_flag) break;
+      const uint64_t t_wait = MGW_DIAG_NOW();
       if (!mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
         *abort_flag = 1;
         if (lane == 0 && args.status) atomicOr(args.status, kDevTimeout);
@@ -337,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       const int row0 = s_off[item.e] + item.rt * BM;
       const int valid = min(BM, s_off[item.e + 1] - row0);
       store_acc_rows(args, tmem, quarter, lane, row0, valid, item.kt * BN, BN);
+      if (warp == 0 && lane == 0) MGW_DIAG_ITEM(dgrad, it, t_wait, MGW_DIAG_NOW());
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);

@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "diag.cuh"
 #include "kernels.h"
 
 namespace mgw {
@@ -117,6 +118,9 @@ __device__ __forceinline__ void store_acc_rows(const DgradArgs& args, uint32_t t
                                                uint32_t lane, int row0, int valid, int col0,
                                                int ncols) {
   if (quarter * 32 >= valid) return;
+  if (!MGW_DIAG_CHECK(row0 >= 0 && row0 + valid <= args.rows && col0 >= 0 && col0 + ncols <= args.in_f,
+                      lane == 0 ? args.status : nullptr))
+    return;
   const int r = quarter * 32 + static_cast<int>(lane);
   float* dst = args.dx + static_cast<size_t>(row0 + (r < valid ? r : 0)) * args.in_f + col0;
   const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16);

@@ -28,6 +28,9 @@
 #include "dgrad.cuh"
 
 namespace mgw {
+
+MGW_DIAG_TIMELINE_DEFINE(dgrad_pair, 3)
+
 namespace {
 
 using namespace dgrad;
@@ -211,6 +214,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = bar_raw_full(rs);
           const uint32_t dst = sbase + kOffRaw + rs * kRawBytes;
           mbar_arrive_expect_tx(fb, kRawBytes);
+          (void)MGW_DIAG_CHECK(item.e * out_f + (c + 1) * BK <= E * out_f &&
+                                   item.kt * BNP + k_half + kHalfN <= in_f && (c + 1) * BK <= out_f,
+                               args.status);
           tma_load_2d(dst, &args.tm_w, item.kt * BNP + k_half, item.e * out_f + c * BK, fb);
           tma_load_2d(dst + kRawW, &args.tm_dy, c * BK, row0, fb);
           --ahead;
@@ -329,6 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (*abort_flag) break;
+      const uint64_t t_wait = MGW_DIAG_NOW();
       if (!mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
         if (lane == 0) abort_both();
         break;
@@ -339,6 +346,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int row0 = s_off[item.e] + item.rt * 2 * BM + BM * static_cast<int>(rank);
       const int valid = min(BM, s_off[item.e + 1] - row0);  // may be <= 0 for the odd CTA
       store_acc_rows(args, tmem, quarter, lane, row0, valid, item.kt * BNP, BNP);
+      if (warp == 0 && lane == 0) MGW_DIAG_ITEM(dgrad_pair, it, t_wait, MGW_DIAG_NOW());
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(acc_empty0);

@@ -48,6 +48,7 @@ struct WgradArgs {
   const uint8_t* xs;   // x scale atoms
   const int32_t* expert_off;
   int E, M, N, K;
+  long long mcap;      // token capacity of the quantized operands (bounds checks of the diag build)
   int* status;
   // Test hook for the device time limit: when set, the static kernel's producer announces
   // its first chunk's bytes but never issues the copies, so the waits on that stage run out
@@ -120,5 +121,22 @@ cudaError_t launch_grouped_dgrad(const DgradArgs& a, int num_sms, cudaStream_t s
 // enough of them to keep the SM pairs busy; tm_w's box is then 128 columns x 32 rows.
 bool dgrad_uses_pair(const DgradArgs& a, int num_sms);
 cudaError_t launch_grouped_dgrad_pair(const DgradArgs& a, int num_sms, cudaStream_t stream);
+
+// Work-item timeline of the diagnostic library (libmgw_diag.so, compiled with MGW_DIAG): one
+// record per CTA and work item, the layout of mgw_diag_record in include/mgw_diag.h.
+struct DiagRecord {
+  uint32_t kernel, sm, cta, pad;
+  long long item;
+  uint64_t t_wait, t_done;
+};
+constexpr int kDiagTimelineCap = 65536;  // records kept per kernel family
+#ifdef MGW_DIAG
+cudaError_t diag_timeline_read_wgrad(DiagRecord* host, int cap, int* count);
+cudaError_t diag_timeline_reset_wgrad();
+cudaError_t diag_timeline_read_dgrad(DiagRecord* host, int cap, int* count);
+cudaError_t diag_timeline_reset_dgrad();
+cudaError_t diag_timeline_read_dgrad_pair(DiagRecord* host, int cap, int* count);
+cudaError_t diag_timeline_reset_dgrad_pair();
+#endif
 
 }  // namespace mgw

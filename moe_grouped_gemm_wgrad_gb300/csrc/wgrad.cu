@@ -29,9 +29,13 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "diag.cuh"
 #include "kernels.h"
 
 namespace mgw {
+
+MGW_DIAG_TIMELINE_DEFINE(wgrad, 1)
+
 namespace {
 
 constexpr int BM = 128;  // grad_w rows per tile (MMA M)
@@ -575,6 +579,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           const uint32_t fb = full0_leader + 8u * stage;  // the even CTA's full barrier
           const uint32_t sa = sbase + stage * kPStageBytes;
           const int ch = ch0 + c;
+          (void)MGW_DIAG_CHECK(static_cast<long long>(ch + 1) * BT <= args.mcap && arow + 128 <= N &&
+                                   brow + 128 <= K,
+                               args.status);
           tma_load_2d_pair(sa, &args.tm_a, ch * BT, arow, fb);
           tma_load_2d_pair(sa + kPABytes, &args.tm_b, ch * BT, brow, fb);
           // this CTA's g atom and both x atoms of the K tile (every CTA's accumulator spans
@@ -700,6 +707,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int np = tile / tiles_k, kt = tile % tiles_k;
       uint8_t* base = out + (static_cast<size_t>(e) * N + np * 256 + 128 * rank) * pitch +
                       static_cast<size_t>(kt) * BN * 2 + lane * 16;
+      if (!MGW_DIAG_CHECK(np * 256 + 128 * static_cast<int>(rank) + BM <= N && (kt + 1) * BN <= K,
+                          args.status))
+        continue;
 #pragma unroll 4
       for (int r = 0; r < BM; ++r) st_global_zero16_hint(base + r * pitch, zpol);
     }
@@ -724,6 +734,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       uint32_t pk[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) pk[j] = 0u;
+      const uint64_t t_wait = MGW_DIAG_NOW();
       if (!*abort_flag) {
         if (mbar_wait(bar_acc_full, acc_phase, abort_flag)) {
           tc_fence_after();
@@ -748,6 +759,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       const uint32_t stage_base = sbase + kPOffOut;
       const int orow = e * N + np * 256 + 128 * static_cast<int>(rank);
+      const bool in_out = MGW_DIAG_CHECK(np * 256 + 128 * static_cast<int>(rank) + 128 <= N &&
+                                             kt * BN + 256 <= K,
+                                         store_leader ? args.status : nullptr);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         if (store_leader) bulk_wait_read0();
@@ -762,11 +776,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           fence_async_smem();
         }
         named_bar_sync(1, kEpiWarps * 32);
-        if (store_leader && !*abort_flag) {
+        if (store_leader && !*abort_flag && in_out) {
           tma_store_2d_hint(&args.tm_out, kt * BN + 64 * b, orow, stage_base, opol);
           bulk_commit();
         }
       }
+      if (store_leader) MGW_DIAG_ITEM(wgrad, it, t_wait, MGW_DIAG_NOW());
     }
     if (store_leader) bulk_wait0();
   }

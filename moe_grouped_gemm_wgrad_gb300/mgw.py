@@ -13,6 +13,7 @@ with the operands' device current.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -21,11 +22,16 @@ import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmgw.so")
+# The diagnostic build (include/mgw_diag.h): same results, plus a work-item timeline and
+# device bounds checks.  Only diagnostic_library() switches the binding to it.
+LIB_DIAG_PATH = os.path.join(HERE, "libmgw_diag.so")
 
 MGW_OK = 0
 MGW_DEV_BAD_OFFSETS = 1
 MGW_DEV_TIMEOUT = 2
 MGW_DEV_BAD_INDEX = 4
+MGW_DEV_BOUNDS = 8   # diagnostic library only
+DIAG_KERNELS = {1: "grouped_wgrad_pair_kernel", 2: "grouped_dgrad_kernel", 3: "grouped_dgrad_pair_kernel"}
 MAX_EXPERTS = 1024
 SCALE_FLOOR = 0      # OCP MX rule 2^(floor(log2 amax) - 8)
 SCALE_CEIL_448 = 1   # the post-attn page's RoundUp rule ceil_pow2(amax / 448)
@@ -39,8 +45,18 @@ EXPORTS = (
 )
 
 
+DIAG_EXPORTS = ("mgw_diag_timeline", "mgw_diag_timeline_reset")
+
+
 class MgwError(RuntimeError):
     pass
+
+
+class DiagRecord(ctypes.Structure):
+    """mgw_diag_record of include/mgw_diag.h."""
+    _fields_ = [("kernel", ctypes.c_uint32), ("sm", ctypes.c_uint32), ("cta", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32), ("item", ctypes.c_int64),
+                ("t_wait_ns", ctypes.c_uint64), ("t_done_ns", ctypes.c_uint64)]
 
 
 _lock = threading.Lock()
@@ -79,6 +95,61 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, SZ, P, P, P]
     lib.mgw_grouped_wgrad_mxfp8_balanced_noalloc.restype = I
     return lib
+
+
+def bind_diag(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """bind() plus the two entry points only the diagnostic library exports."""
+    bind(lib)
+    lib.mgw_diag_timeline.argtypes = [ctypes.POINTER(DiagRecord), ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_int)]
+    lib.mgw_diag_timeline.restype = ctypes.c_int
+    lib.mgw_diag_timeline_reset.argtypes = []
+    lib.mgw_diag_timeline_reset.restype = ctypes.c_int
+    return lib
+
+
+_diag_lib = None
+
+
+@contextlib.contextmanager
+def diagnostic_library():
+    """Runs the calls made inside the block through libmgw_diag.so (built beside libmgw.so):
+    the same results, a work-item timeline (diag_timeline) and device bounds checks that set
+    MGW_DEV_BOUNDS in a call's status word.  Not thread-safe against concurrent calls made
+    outside the block."""
+    global _lib, _diag_lib
+    with _lock:
+        if _diag_lib is None:
+            if not os.path.exists(LIB_DIAG_PATH):
+                raise MgwError(f"{LIB_DIAG_PATH} is not built; run `python -m moe_grouped_gemm_wgrad_gb300.build`")
+            _diag_lib = bind_diag(ctypes.CDLL(LIB_DIAG_PATH))
+        prev, _lib = _lib, _diag_lib
+    try:
+        yield _diag_lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def diag_timeline(cap: int = 3 * 65536) -> list[dict]:
+    """The work-item timeline recorded by the diagnostic library since the last
+    diag_timeline_reset(), one dict per (CTA, item); synchronises with the device."""
+    if _diag_lib is None:
+        raise MgwError("diag_timeline needs diagnostic_library() to have been entered")
+    buf = (DiagRecord * cap)()
+    total = ctypes.c_int(0)
+    _check(_diag_lib.mgw_diag_timeline(buf, cap, ctypes.byref(total)), "mgw_diag_timeline")
+    out = []
+    for r in buf[:min(cap, total.value)]:
+        out.append({"kernel": DIAG_KERNELS.get(r.kernel, str(r.kernel)), "sm": r.sm, "cta": r.cta,
+                    "item": r.item, "t_wait_ns": r.t_wait_ns, "t_done_ns": r.t_done_ns})
+    return out
+
+
+def diag_timeline_reset() -> None:
+    if _diag_lib is None:
+        raise MgwError("diag_timeline_reset needs diagnostic_library() to have been entered")
+    _check(_diag_lib.mgw_diag_timeline_reset(), "mgw_diag_timeline_reset")
 
 
 def load() -> ctypes.CDLL:

@@ -169,3 +169,43 @@ def test_header_is_self_contained_c_and_cxx(lang, std):
                           "-pedantic", "-fsyntax-only", "-I", os.path.join(ROOT, "include"), "-"],
                          input=src, capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stderr
+
+
+def _diag_declared_functions():
+    text = open(os.path.join(ROOT, "include", "mgw_diag.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mgw_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_diagnostic_library_exports_and_the_product_does_not(lib):
+    """libmgw_diag.so exports every function of mgw.h and mgw_diag.h; libmgw.so exports
+    none of mgw_diag.h's (the diagnostics are not in the product library)."""
+    diag = _diag_declared_functions()
+    assert set(diag) == set(mgw.DIAG_EXPORTS), diag
+    dlib = ctypes.CDLL(build.LIB_DIAG)
+    for name in _declared_functions() + diag:
+        assert hasattr(dlib, name), name
+    for name in diag:
+        assert not hasattr(lib, name), name
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_diag_header_is_self_contained(lang, std):
+    import shutil
+    import subprocess
+
+    compiler = "gcc" if lang == "c" else "g++"
+    if shutil.which(compiler) is None:
+        pytest.skip(f"{compiler} not available")
+    uses = "\n".join(f"  (void)&{name};" for name in _diag_declared_functions())
+    src = (f'#include "mgw_diag.h"\nint main(void) {{\n{uses}\n'
+           f'  mgw_diag_record r; (void)r;\n  return MGW_DEV_BOUNDS == 8 ? MGW_OK : 1;\n}}\n')
+    out = subprocess.run([compiler, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-Werror",
+                          "-pedantic", "-fsyntax-only", "-I", os.path.join(ROOT, "include"), "-"],
+                         input=src, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+
+
+def test_diag_record_layout_matches_header():
+    assert ctypes.sizeof(mgw.DiagRecord) == 40
+    assert mgw.DiagRecord.item.offset == 16 and mgw.DiagRecord.t_done_ns.offset == 32
