@@ -96,3 +96,59 @@ def test_noalloc_more_than_64_tiles_per_expert_schedules_without_splits():
     oops = oracle_quantize_by_expert(case.g_bf16, case.expert_off, Mcap)
     oops += oracle_quantize_by_expert(case.x_bf16, case.expert_off, Mcap)
     check_wgrad_full(out, oops, case.expert_off, case.N, case.K)
+
+
+def test_noalloc_in_a_second_context_and_back():
+    """The library looks its workspace up per CUDA context: with a second (non-primary)
+    driver context current, a call on buffers of that context uses that context's copy of
+    the array, and the next call back in the primary context uses the primary's again.  The
+    three results are the same bits."""
+    import ctypes
+
+    case = synth.wgrad_random(7000, 256, 256, [1000, 2000, 0, 4000], seed=61)
+    ops = _operands(case)
+    out = torch.empty((case.E * case.N, case.K), dtype=torch.bfloat16, device="cuda")
+    first = _call(case, ops, out).clone()
+    host = [t.cpu().contiguous() for t in ops]  # off, gq, gs, xq, xs
+    Mcap = mgw.token_capacity(case.M, case.E)
+    cu = ctypes.CDLL("libcuda.so.1")
+    dev = ctypes.c_int()
+    assert cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+    ctx = ctypes.c_void_p()
+    assert cu.cuCtxCreate_v2(ctypes.byref(ctx), 0, dev) == 0  # pushed: now current
+    ptrs = []
+    try:
+        def dalloc(nbytes):
+            p = ctypes.c_uint64()
+            assert cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(nbytes)) == 0
+            ptrs.append(p)
+            return p
+
+        dops = []
+        for t in host:
+            nbytes = t.numel() * t.element_size()
+            p = dalloc(nbytes)
+            assert cu.cuMemcpyHtoD_v2(p, ctypes.c_void_p(t.data_ptr()), ctypes.c_size_t(nbytes)) == 0
+            dops.append(p)
+        d_off, d_gq, d_gs, d_xq, d_xs = dops
+        d_out = dalloc(out.numel() * 2)
+        d_status = dalloc(4)
+        assert cu.cuMemsetD32_v2(d_status, ctypes.c_uint(0), ctypes.c_size_t(1)) == 0
+        V = lambda p: ctypes.c_void_p(p.value)  # noqa: E731
+        rc = mgw.load().mgw_grouped_wgrad_mxfp8_balanced_noalloc(
+            V(d_gq), V(d_gs), V(d_xq), V(d_xs), V(d_off), case.E, case.M, case.N, case.K, Mcap,
+            V(d_out), V(d_status), None)
+        assert rc == 0, rc
+        assert cu.cuCtxSynchronize() == 0
+        got = torch.empty((case.E * case.N, case.K), dtype=torch.int16)
+        status = ctypes.c_int(-1)
+        assert cu.cuMemcpyDtoH_v2(ctypes.c_void_p(got.data_ptr()), d_out, ctypes.c_size_t(got.numel() * 2)) == 0
+        assert cu.cuMemcpyDtoH_v2(ctypes.byref(status), d_status, ctypes.c_size_t(4)) == 0
+        assert status.value == 0
+        assert torch.equal(got, first.view(torch.int16).cpu())
+    finally:
+        for p in ptrs:
+            cu.cuMemFree_v2(p)
+        assert cu.cuCtxDestroy_v2(ctx) == 0  # popped: the primary context is current again
+    again = _call(case, ops, torch.empty_like(out))
+    assert torch.equal(again.view(torch.int16), first.view(torch.int16))
