@@ -113,3 +113,19 @@ def test_dgrad_wide_pair_tiles_ragged():
     ref, bound = oracle_dgrad_threads(case.dy, case.W, case.expert_off)
     bad = np.argwhere(~(np.abs(dx - ref) <= 1e-5 * bound))
     assert bad.size == 0, (len(bad), bad[:5].tolist())
+
+
+@pytest.mark.parametrize("counts,out_f,in_f", [
+    ([0, 1, 300, 0, 2, 511], 32, 512),                       # single-SM kernel, one 32-wide chunk
+    ([0, 1, 3000, 0, 2, 2500, 1, 0], 32, 4096),              # CTA pairs, one 32-wide chunk
+    ([1, 255, 256, 257, 0, 513, 1023, 1], 64, 8192),         # CTA pairs, tile-edge counts
+], ids=["single_sm_one_chunk", "pairs_one_chunk", "pairs_tile_edges"])
+def test_dgrad_edge_shapes(counts, out_f, in_f):
+    """Shortest reduction (one raw chunk: two 16-wide operand stages), one-row and empty
+    experts at both ends, counts one off the 128- and 256-row tile edges; on both kernels
+    (the pair kernel when there are at least four rounds of 256-row pair tiles)."""
+    case = synth.dgrad_random(sum(counts), out_f, in_f, counts, seed=38)
+    dx = _gpu_dgrad(case).cpu().numpy().astype(np.float64)
+    ref, bound = oracle_dgrad_threads(case.dy, case.W, case.expert_off)
+    bad = np.argwhere(~(np.abs(dx - ref) <= 1e-5 * bound))
+    assert bad.size == 0, (len(bad), bad[:5].tolist())
