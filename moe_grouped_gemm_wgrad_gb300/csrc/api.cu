@@ -454,6 +454,13 @@ mgw_status mgw_grouped_dgrad_f32(const float* dy, const float* W, const int32_t*
                    rows > 0 ? static_cast<uint64_t>(rows) : 1, static_cast<uint64_t>(out_f) * 4,
                    32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return MGW_ERR_CUDA;
+#ifdef MGW_TEST_HOOKS
+  {
+    // Only in the test build of the library (libmgw_testhooks.so), see kernels.h.
+    const char* v = std::getenv("MGW_TEST_DROP_LOAD");
+    a.drop_first_load = (v != nullptr && v[0] == '1') ? 1 : 0;
+  }
+#endif
   const cudaError_t err =
       pair ? mgw::launch_grouped_dgrad_pair(a, dev.sms, static_cast<cudaStream_t>(stream))
            : mgw::launch_grouped_dgrad(a, dev.sms, static_cast<cudaStream_t>(stream));

@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
       uint32_t pending_phase[kRawStages];
       for (int s = 0; s < kRawStages; ++s) pending[s] = 0, pending_phase[s] = 0;
       bool ok = true;
+      bool dropped = false;
       // L2 prefetch cursor over this CTA's (item, chunk) sequence, kPrefetch chunks ahead of
       // the loads: the two-stage ring alone leaves each load a DRAM round trip to hide.
       long long pf_it = blockIdx.x;
@@ -203,6 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_dgrad_kernel(const __grid
           const uint32_t fb = bar_raw_full(rs);
           const uint32_t dst = sbase + kOffRaw + rs * kRawBytes;
           mbar_arrive_expect_tx(fb, kRawBytes);
+          if (args.drop_first_load && !dropped) {  // test hook: this stage never fills
+            dropped = true;
+            pending[rs] = 1;
+            pending_phase[rs] = rph;
+            if (++rs == kRawStages) rs = 0, rph ^= 1u;
+            continue;
+          }
           (void)MGW_DIAG_CHECK(item.e * out_f + (c + 1) * BK <= E * out_f &&
                                    (item.kt + 1) * BN <= in_f && (c + 1) * BK <= out_f &&
                                    row0 < args.rows,

@@ -174,6 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pending_phase[kRawStages];
       for (int s = 0; s < kRawStages; ++s) pending[s] = 0, pending_phase[s] = 0;
       bool ok = true;
+      bool dropped = false;
       const int k_half = kHalfN * static_cast<int>(rank);
       const int r_half = BM * static_cast<int>(rank);
       // L2 prefetch cursor over this pair's (item, chunk) sequence, kPrefetch chunks ahead of
@@ -214,6 +215,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = bar_raw_full(rs);
           const uint32_t dst = sbase + kOffRaw + rs * kRawBytes;
           mbar_arrive_expect_tx(fb, kRawBytes);
+          if (args.drop_first_load && !dropped) {  // test hook: this stage never fills
+            dropped = true;
+            pending[rs] = 1;
+            pending_phase[rs] = rph;
+            if (++rs == kRawStages) rs = 0, rph ^= 1u;
+            continue;
+          }
           (void)MGW_DIAG_CHECK(item.e * out_f + (c + 1) * BK <= E * out_f &&
                                    item.kt * BNP + k_half + kHalfN <= in_f && (c + 1) * BK <= out_f,
                                args.status);

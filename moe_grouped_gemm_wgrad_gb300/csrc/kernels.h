@@ -114,6 +114,9 @@ struct DgradArgs {
   int E, rows, out_f, in_f;
   int* status;
   int dx_align32;      // dx is 32-byte aligned: the epilogue stores whole 32-byte sectors
+  // Test hook for the device time limit, as in WgradArgs: the producer announces its first
+  // raw stage's bytes but never issues the copies.  Only libmgw_testhooks.so sets it.
+  int drop_first_load;
 };
 cudaError_t launch_grouped_dgrad(const DgradArgs& a, int num_sms, cudaStream_t stream);
 

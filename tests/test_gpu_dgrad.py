@@ -2,6 +2,8 @@
 
 Tolerance (from the workload definition): |gpu - ref| <= 1e-5 * sum_n |dy||W|.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -129,3 +131,35 @@ def test_dgrad_edge_shapes(counts, out_f, in_f):
     ref, bound = oracle_dgrad_threads(case.dy, case.W, case.expert_off)
     bad = np.argwhere(~(np.abs(dx - ref) <= 1e-5 * bound))
     assert bad.size == 0, (len(bad), bad[:5].tolist())
+
+
+@pytest.mark.parametrize("counts,out_f,in_f", [
+    ([100, 0, 156], 64, 256),                      # single-SM kernel
+    ([0, 1, 3000, 0, 2, 2500, 1, 0], 32, 4096),    # CTA pairs
+], ids=["single_sm", "cta_pairs"])
+def test_dgrad_device_time_limit_reports_and_context_survives(monkeypatch, counts, out_f, in_f):
+    """A raw stage that never fills makes the dgrad kernel's bounded waits run out: the call
+    reports MGW_DEV_TIMEOUT in the status word instead of hanging, and the context stays
+    usable.  The stage is dropped by the test build of the library (libmgw_testhooks.so,
+    MGW_TEST_DROP_LOAD=1); libmgw.so has no such switch."""
+    from moe_grouped_gemm_wgrad_gb300 import build
+
+    hooks = mgw.bind(ctypes.CDLL(build.LIB_TESTHOOKS))
+    case = synth.dgrad_random(sum(counts), out_f, in_f, counts, seed=39)
+    dy = torch.from_numpy(case.dy).cuda()
+    W = torch.from_numpy(case.W).cuda()
+    off = dev_i32(case.expert_off)
+    dx = torch.zeros((case.rows, case.in_f), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    monkeypatch.setenv("MGW_TEST_DROP_LOAD", "1")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = hooks.mgw_grouped_dgrad_f32(p(dy), p(W), p(off), case.E, case.rows, case.out_f, case.in_f,
+                                     p(dx), p(status),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == mgw.MGW_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) & mgw.MGW_DEV_TIMEOUT
+    # the product library ignores the variable, and the next call is correct
+    got = _gpu_dgrad(case).cpu().numpy().astype(np.float64)
+    ref, bound = oracle_dgrad_threads(case.dy, case.W, case.expert_off)
+    assert (np.abs(got - ref) <= 1e-5 * bound).all()
