@@ -2,9 +2,9 @@
 // [C, Mcap] (token-contiguous, per-expert 128-padded) + e8m0 scale atoms.
 //
 // HBM-bound transpose-quantize.  One work unit is 128 padded tokens x 128
-// features.  A persistent grid walks the units; each CTA keeps two units' bf16
-// tiles (32 KB each) in flight with TMA loads, so HBM reads overlap the
-// conversion of the previous unit.  Per unit every thread owns one pair of
+// features.  A persistent grid walks the units; each CTA has two units' bf16
+// tiles (32 KB each) in its input ring and refills a stage as soon as its values
+// are in registers, so HBM reads overlap the conversion of the unit just read.  Per unit every thread owns one pair of
 // adjacent features and one 32-token block: 32-bit shared-memory reads, the
 // block maximum from the bf16 bits, an exact power-of-two scale, the hardware's
 // round-to-nearest-even saturating e4m3 convert.  The e4m3 tile (128B-swizzled) and
@@ -215,6 +215,10 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
       amax_lo = max(amax_lo, v[i] & 0x7FFFu);                // |bf16| orders like its bits
       amax_hi = max(amax_hi, (v[i] >> 16) & 0x7FFFu);
     }
+    // Every value of the stage went into the block maxima, so the stage is read: refill it
+    // now, and the load overlaps this unit's conversion.
+    __syncthreads();
+    if (tid < 32 && nu < units) fire(next, stage);
     float inv_lo, inv_hi;
     int byte_lo = scale_byte(amax_lo, rule, &inv_lo);
     int byte_hi = scale_byte(amax_hi, rule, &inv_hi);
@@ -231,8 +235,7 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     }
     // The store issued from this output buffer two units ago must have read it.
     if (tid == 0) bulk_wait_read1();
-    __syncthreads();  // input stage `stage` fully read; output buffer `ob` free
-    if (tid < 32 && nu < units) fire(next, stage);
+    __syncthreads();  // output buffer `ob` free
     {
       // 128 feature rows x 128 token bytes, 16-byte chunk j of row r at (j ^ (r % 8)).
       const uint32_t obase = sbase + kOffOut + ob * kOutBuf;
