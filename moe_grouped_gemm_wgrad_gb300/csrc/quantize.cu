@@ -4,12 +4,16 @@
 // HBM-bound transpose-quantize.  One work unit is 128 padded tokens x 128
 // features.  A persistent grid walks the units; each CTA has two units' bf16
 // tiles (32 KB each) in its input ring and refills a stage as soon as its values
-// are in registers, so HBM reads overlap the conversion of the unit just read.  Per unit every thread owns one pair of
-// adjacent features and one 32-token block: 32-bit shared-memory reads, the
-// block maximum from the bf16 bits, an exact power-of-two scale, the hardware's
-// round-to-nearest-even saturating e4m3 convert.  The e4m3 tile (128B-swizzled) and
-// its 512-byte scale atom leave through a double-buffered staging area with TMA
-// bulk stores, so the CTA goes on to the next unit while they drain.
+// are in registers, so HBM reads overlap the conversion of the unit just read.  The
+// lane that issues a stage's load also publishes the unit's token count with it, and
+// the unit coordinates step with the grid stride, so a unit costs the consumers no
+// search and no division.  Per unit every thread owns one pair of adjacent features
+// and one 32-token block: 32-bit shared-memory reads, both block maxima at once with a
+// packed bf16 magnitude max, an exact power-of-two scale applied by packed fp32x2
+// multiplies, the hardware's round-to-nearest-even saturating e4m3 convert.  The e4m3
+// tile (128B-swizzled) and its 512-byte scale atom leave through a double-buffered
+// staging area with TMA bulk stores, so the CTA goes on to the next unit while they
+// drain.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -30,6 +34,7 @@ constexpr int kOutBuf = 17408;           // tile + scale atom, padded to 1024 B
 constexpr int kOffOut = kInStages * kInBytes;
 constexpr int kOffBar = kOffOut + 2 * kOutBuf;
 constexpr int kOffTable = kOffBar + 8 * kInStages + 16;
+static_assert(kInStages <= 2, "misc area: flag, abort, one token count per stage");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -42,6 +47,21 @@ __device__ __forceinline__ void bulk_store_1d(void* gdst, uint32_t ssrc, uint32_
                    reinterpret_cast<uint64_t>(gdst)),
                "r"(ssrc), "r"(bytes)
                : "memory");
+}
+// Running largest magnitude of each bf16 half of m and v, lane by lane.  The sign of the
+// result is meaningless (the caller clears it); a NaN in either input gives NaN, whose
+// cleared bits, like any NaN's or an infinity's, carry the all-ones exponent.
+__device__ __forceinline__ uint32_t amax_bf16x2(uint32_t m, uint32_t v) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(v));
+  return r;
+}
+// Two fp32 products a*s, b*s in one packed multiply (each rounded as the scalar one).
+__device__ __forceinline__ void mul_f32x2(uint32_t a, uint32_t b, uint64_t s2, float& x, float& y) {
+  asm("{\n\t.reg .b64 t, r;\n\tmov.b64 t, {%2, %3};\n\tmul.rn.f32x2 r, t, %4;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(x), "=f"(y)
+      : "r"(a), "r"(b), "l"(s2));
 }
 __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -87,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   // 128B-swizzled TMA tiles want 1024-byte alignment; the launch adds the slack.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 8 * kInStages);  // [0] flag [1] abort
+  // [0] flag [1] abort [2 + s] tokens of the expert in the unit loaded into stage s
+  int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 8 * kInStages);
   int* s_off = reinterpret_cast<int*>(smem + kOffTable);
   int* s_pad = s_off + (E + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_misc[1]);
@@ -102,9 +123,10 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   if (!load_offsets(expert_off, E, M, s_off, s_pad, &s_misc[0], status)) return;
 
   const int col_tiles = C / 128;
-  const long long units = (Mcap / 128) * col_tiles;
+  // below 2^31: q holds C x Mcap bytes, 16 KB per unit
+  const int units = static_cast<int>((Mcap / 128) * col_tiles);
   const int used_chunks = s_pad[E] / 128;
-  const long long stride = gridDim.x;
+  const int stride = gridDim.x;
 
   // Loads of unit u into input stage s, issued by warp 0 in two halves so that the
   // gather indices can be fetched early: prep() resolves the unit (and, for a gathered
@@ -119,10 +141,10 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     int ct, valid, bad;
     int rr[4];
   };
-  auto prep = [&](long long u) {
+  auto prep = [&](int u) {
     Pending pd;
-    const int ch = static_cast<int>(u / col_tiles);
-    pd.ct = static_cast<int>(u % col_tiles);
+    const int ch = u / col_tiles;
+    pd.ct = u % col_tiles;
     const Unit un = locate(ch, used_chunks, s_off, s_pad, E);
     pd.valid = un.valid;
     pd.bad = 0;
@@ -146,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   };
   auto fire = [&](const Pending& pd, int s) {
     const uint32_t bar = sbase + kOffBar + 8 * s;
+    // published to the consumers by the arrive's release
+    if (lane == 0) s_misc[2 + s] = pd.valid;
     if (!kGather) {
       if (lane != 0) return;
       if (pd.valid > 0) {
@@ -178,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   };
   if (tid < 32) {
     for (int s = 0; s < kInStages; ++s) {
-      const long long u = blockIdx.x + s * stride;
+      const int u = static_cast<int>(blockIdx.x) + s * stride;
       if (u < units) fire(prep(u), s);
     }
   }
@@ -187,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
   const int kb = tid >> 6;  // 32-token block of the chunk
   uint32_t phase = 0;
   int stage = 0, ob = 0;
-  for (long long u = blockIdx.x; u < units; u += stride) {
-    const int ch = static_cast<int>(u / col_tiles);
-    const int ct = static_cast<int>(u % col_tiles);
-    const Unit un = locate(ch, used_chunks, s_off, s_pad, E);
+  // (chunk, column tile) of unit u, stepped by the grid stride without a division per unit
+  const int step_ch = stride / col_tiles, step_ct = stride % col_tiles;
+  int ch = static_cast<int>(blockIdx.x) / col_tiles, ct = static_cast<int>(blockIdx.x) % col_tiles;
+  for (int u = blockIdx.x; u < units; u += stride) {
     // Every thread waits; the decision to give up is made uniformly for the block.
     const int timed_out = mbar_wait(sbase + kOffBar + 8 * stage, phase, abort_flag) ? 0 : 1;
     if (__syncthreads_or(timed_out)) {
@@ -201,37 +225,49 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
       }
       break;
     }
+    const int valid = s_misc[2 + stage];
     // the unit that will refill this stage: resolve it (and load its indices) now
-    const long long nu = u + kInStages * stride;
+    const int nu = u + kInStages * stride;
     Pending next{0, 0, 0, {0, 0, 0, 0}};
     if (tid < 32 && nu < units) next = prep(nu);
-    const uint32_t* in = reinterpret_cast<const uint32_t*>(smem + stage * kInBytes);
+    const uint32_t* in = reinterpret_cast<const uint32_t*>(smem + stage * kInBytes) + kb * 32 * 64 + p;
     uint32_t v[32];
-    uint32_t amax_lo = 0, amax_hi = 0;
-    const int nvalid = min(32, max(0, un.valid - kb * 32));
+    uint32_t amax = 0;  // block maxima: feature 2p in the low half, 2p+1 in the high half
+    if (valid >= 128) {  // the same branch for the whole CTA
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = (i < nvalid) ? in[(kb * 32 + i) * 64 + p] : 0u;  // bf16 pair (2p low, 2p+1 high)
-      amax_lo = max(amax_lo, v[i] & 0x7FFFu);                // |bf16| orders like its bits
-      amax_hi = max(amax_hi, (v[i] >> 16) & 0x7FFFu);
+      for (int i = 0; i < 32; ++i) {
+        v[i] = in[i * 64];  // bf16 pair (2p low, 2p+1 high)
+        amax = amax_bf16x2(amax, v[i]);
+      }
+    } else {
+      const int nvalid = min(32, max(0, valid - kb * 32));
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = (i < nvalid) ? in[i * 64] : 0u;
+        amax = amax_bf16x2(amax, v[i]);
+      }
     }
+    amax &= 0x7FFF7FFFu;  // |bf16| orders like its bits
     // Every value of the stage went into the block maxima, so the stage is read: refill it
     // now, and the load overlaps this unit's conversion.
     __syncthreads();
     if (tid < 32 && nu < units) fire(next, stage);
     float inv_lo, inv_hi;
-    int byte_lo = scale_byte(amax_lo, rule, &inv_lo);
-    int byte_hi = scale_byte(amax_hi, rule, &inv_hi);
-    if (nvalid == 0) byte_lo = byte_hi = 0;  // a block with no token of the expert: padding
+    int byte_lo = scale_byte(amax & 0xFFFFu, rule, &inv_lo);
+    int byte_hi = scale_byte(amax >> 16, rule, &inv_hi);
+    if (valid <= kb * 32) byte_lo = byte_hi = 0;  // a block with no token of the expert: padding
+    const uint64_t s_lo = (static_cast<uint64_t>(__float_as_uint(inv_lo)) << 32) | __float_as_uint(inv_lo);
+    const uint64_t s_hi = (static_cast<uint64_t>(__float_as_uint(inv_hi)) << 32) | __float_as_uint(inv_hi);
     uint32_t pl[8], ph[8];
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
-      pl[i / 4] = cvt_e4m3x4(__uint_as_float(v[i] << 16) * inv_lo, __uint_as_float(v[i + 1] << 16) * inv_lo,
-                             __uint_as_float(v[i + 2] << 16) * inv_lo, __uint_as_float(v[i + 3] << 16) * inv_lo);
-      ph[i / 4] = cvt_e4m3x4(__uint_as_float(v[i] & 0xFFFF0000u) * inv_hi,
-                             __uint_as_float(v[i + 1] & 0xFFFF0000u) * inv_hi,
-                             __uint_as_float(v[i + 2] & 0xFFFF0000u) * inv_hi,
-                             __uint_as_float(v[i + 3] & 0xFFFF0000u) * inv_hi);
+      float a0, a1, a2, a3, b0, b1, b2, b3;
+      mul_f32x2(v[i] << 16, v[i + 1] << 16, s_lo, a0, a1);
+      mul_f32x2(v[i + 2] << 16, v[i + 3] << 16, s_lo, a2, a3);
+      mul_f32x2(v[i] & 0xFFFF0000u, v[i + 1] & 0xFFFF0000u, s_hi, b0, b1);
+      mul_f32x2(v[i + 2] & 0xFFFF0000u, v[i + 3] & 0xFFFF0000u, s_hi, b2, b3);
+      pl[i / 4] = cvt_e4m3x4(a0, a1, a2, a3);
+      ph[i / 4] = cvt_e4m3x4(b0, b1, b2, b3);
     }
     // The store issued from this output buffer two units ago must have read it.
     if (tid == 0) bulk_wait_read1();
@@ -259,6 +295,9 @@ __global__ void __launch_bounds__(kThreads, 2) mxfp8_quantize_kernel(
     }
     ob ^= 1;
     if (++stage == kInStages) stage = 0, phase ^= 1u;
+    ct += step_ct;
+    ch += step_ch;
+    if (ct >= col_tiles) ct -= col_tiles, ++ch;
   }
   // All bulk stores complete before the CTA exits; loads issued for units this CTA never
   // reached (only after an abort) must land too.
@@ -296,6 +335,7 @@ cudaError_t launch_mxfp8_quantize(const CUtensorMap& tm_src, const CUtensorMap& 
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const long long units = (Mcap / 128) * (C / 128);
+  if (units > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   long long grid = static_cast<long long>(num_sms) * per_sm;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
